@@ -1,0 +1,236 @@
+/*
+ * fm.h -- C ABI of libfm: packed variable-length FlashMask attention and
+ * packed QK RoPE for NVIDIA GB300 (sm_103a).
+ *
+ * Every entry point takes plain pointers and sizes.  Device pointers are
+ * CUDA device addresses of the current device; host pointers are marked.
+ * The caller owns every buffer (inputs, outputs, workspace) and the stream;
+ * the library never allocates device memory, never synchronises the stream
+ * (except fm_get_device_error, which reads one word back) and keeps no
+ * state beyond cached device attributes and resolved driver entry points.
+ * `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ * stream.  All kernels are enqueued on `stream` in call order.
+ *
+ * Packed layout (Unsloth packing blog, section "Why padding is needed";
+ * Varlen-Packing technical document, section 1.1): documents are
+ * concatenated along the token axis with no padding, T tokens in all;
+ * cu_seqlens is int32[n_seqs + 1] on the device with cu[0] = 0,
+ * cu[n_seqs] = T and cu non-decreasing.  Sample s owns tokens
+ * [cu[s], cu[s+1]).  Malformed cu_seqlens never makes a kernel read or write
+ * outside the buffers described here (indices are clamped), but the results
+ * are then unspecified and fm_attn_fwd_varlen sets FM_DEVERR_DATA.
+ *
+ * Tensors are bfloat16, token-major: q[T][Hq][D], k and v[T][Hkv][D].
+ *
+ * Errors: every call validates its arguments on the host first and returns
+ * before any launch when they are invalid; a failed launch returns
+ * FM_ERR_CUDA.  Kernels never trap: conditions only the device can see are
+ * written to a device error word (see fm_get_device_error).
+ */
+#ifndef FM_H_
+#define FM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FM_API __attribute__((visibility("default")))
+#else
+#define FM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fm_status {
+  FM_OK = 0,
+  FM_ERR_INVALID_ARG = 1,  /* null pointer, negative size, inconsistent sizes */
+  FM_ERR_UNSUPPORTED = 2,  /* head_dim / tile shape / device not supported    */
+  FM_ERR_ALIGNMENT = 3,    /* a pointer or stride breaks the 16-byte rule     */
+  FM_ERR_WORKSPACE = 4,    /* output or workspace capacity too small          */
+  FM_ERR_CUDA = 5,         /* a CUDA runtime / driver call failed             */
+  FM_ERR_TIMEOUT = 6,      /* a bounded device wait ran out (see below)       */
+  FM_ERR_DEVICE_DATA = 7   /* the device saw malformed cu_seqlens             */
+} fm_status;
+
+/* Bits of the device error word. */
+#define FM_DEVERR_TIMEOUT 0x1u /* a pipeline wait exceeded its limit      */
+#define FM_DEVERR_DATA 0x2u    /* malformed cu_seqlens seen on the device  */
+
+/* Flags. */
+#define FM_FLAG_FORCE_INT64 0x1u /* use the 64-bit index specialisation */
+
+/*
+ * fm_rope_qk_varlen -- rotary position embedding of q and k, in place, with
+ * positions restarting at every packed sample.
+ *
+ * Unsloth packing blog, section "Fused QK RoPE Triton kernel with packing":
+ * one launch rotates both q and k (no clones, no transposes), with
+ * Y = X*cos + rotate_half(X)*sin, rotate_half(X) = X @ R, R = [[0, I], [-I, 0]];
+ * the backward pass is the same rotation with sin -> -sin.  Section
+ * "Uncontaminated packing": position ids reset per sample, so token t of
+ * sample s has position p = t - cu[s].  Channel i pairs with channel
+ * i + D/2; the angle of pair i is p * theta^(-2i/D).
+ *
+ *   q, k            device bf16, rotated in place.  Token t, head h of q is
+ *                   at q + t*q_token_stride + h*head_dim (elements); heads
+ *                   are contiguous.  q and k may be views into one fused
+ *                   buffer as long as they do not overlap.
+ *   total_tokens    T >= 0 (T = 0 is a no-op).
+ *   n_heads_q/kv    >= 1 (n_heads_kv = 0 skips k, which may then be NULL).
+ *   head_dim        64 or 128.
+ *   *_token_stride  elements between consecutive tokens, >= heads*head_dim,
+ *                   multiple of 8 (16 bytes).
+ *   cu_seqlens      device int32[n_seqs + 1]; n_seqs >= 1.  A sample may be
+ *                   at most 2^24 tokens long (positions are exact in fp32).
+ *   theta           RoPE base, > 0.
+ *   backward        0: forward rotation, 1: inverse rotation (sin -> -sin).
+ *   flags           FM_FLAG_FORCE_INT64 or 0 (64-bit offsets are also chosen
+ *                   automatically when an element offset reaches 2^31).
+ *   q, k must be 16-byte aligned.
+ */
+FM_API fm_status fm_rope_qk_varlen(void* q, void* k, int64_t total_tokens, int n_heads_q,
+                            int n_heads_kv, int head_dim, int64_t q_token_stride,
+                            int64_t k_token_stride, const int32_t* cu_seqlens, int n_seqs,
+                            double theta, int backward, uint32_t flags, void* stream);
+
+/*
+ * fm_num_kv_tiles_bound -- number of per-tile slots used by the block
+ * statistics layout below: floor(T / block_n) + n_seqs.
+ *
+ * Tiles are sample-local: tile j of sample s covers key columns
+ * [cu[s] + j*block_n, min(cu[s] + (j+1)*block_n, cu[s+1])) and lives in slot
+ * floor(cu[s] / block_n) + s + j.  Distinct tiles never share a slot and no
+ * slot reaches the bound; slots that hold no tile are filled with
+ * (INT32_MAX, INT32_MIN) pairs.  Returns -1 on invalid arguments.
+ */
+FM_API int64_t fm_num_kv_tiles_bound(int64_t total_tokens, int n_seqs, int block_n);
+
+/*
+ * fm_mask_block_minmax -- FlashMask preprocessing: the eight per-key-tile
+ * extreme vectors.
+ *
+ * PaddleNLP FlashMask article, section 2.2: the mask is given column by
+ * column as LTS/LTE (rows [LTS_j, LTE_j) masked on and below the diagonal)
+ * and UTS/UTE (rows [UTS_j, UTE_j) masked above it), global row indices.
+ * Section 3.1: split the columns by the attention kernel's key tile and take
+ * the minimum and maximum of each vector over every tile.
+ *
+ *   startend_row_indices  device int32[n_mask_heads][4][T], vectors in the
+ *                         order LTS, LTE, UTS, UTE.
+ *   n_mask_heads          >= 1.
+ *   block_n               key tile width, 64 or 128.
+ *   block_minmax          device int32[n_mask_heads][8][n_slots] output,
+ *                         n_slots = fm_num_kv_tiles_bound(T, n_seqs, block_n);
+ *                         the eight rows are LTS min, LTS max, LTE min,
+ *                         LTE max, UTS min, UTS max, UTE min, UTE max.
+ *   block_minmax_capacity elements available at block_minmax; must be at
+ *                         least n_mask_heads * 8 * n_slots.
+ */
+FM_API fm_status fm_mask_block_minmax(const int32_t* startend_row_indices, int n_mask_heads,
+                               int64_t total_tokens, const int32_t* cu_seqlens, int n_seqs,
+                               int block_n, int32_t* block_minmax,
+                               int64_t block_minmax_capacity, void* stream);
+
+/*
+ * fm_attn_fwd_workspace_size -- bytes of device workspace that
+ * fm_attn_fwd_varlen needs for these sizes (scheduler tables, counters and
+ * the device error word).  Returns 0 on invalid arguments.
+ */
+FM_API size_t fm_attn_fwd_workspace_size(int64_t total_tokens, int n_seqs, int n_heads_q, int block_m);
+
+/*
+ * fm_attn_fwd_varlen -- FlashMask attention forward over packed samples.
+ *
+ * PaddleNLP FlashMask article, section 3: FlashAttention-2 tiling (Q tiles
+ * of block_m rows, key/value tiles of block_n columns, online softmax, S and
+ * P kept on chip) in which every (Q tile, KV tile) block is classified from
+ * the eight statistics (section 3.2) as fully masked (skipped), partially
+ * masked (element mask applied) or unmasked (no mask arithmetic); section
+ * 3.3: the result equals attention under the dense mask.  For every sample
+ * s, q head h and row i of s:
+ *     o_i   = sum_j softmax_j(scale * q_i . k_j) v_j   over unmasked keys j of s
+ *     lse_i = log sum_j exp(scale * q_i . k_j)         (natural log)
+ * with key/value head h / (Hq / Hkv).  Element (i, j), i >= j (diagonal
+ * included) is masked iff LTS_j <= i < LTE_j; element i < j is masked iff
+ * causal or UTS_j <= i < UTE_j; keys of other samples are always masked.
+ * A row with no unmasked key gets o = 0 and lse = -inf.  Section 3.4 names
+ * softmax_lse as an input of the backward operator, hence the lse output.
+ *
+ * Scheduling (Varlen-Packing technical document, section 2, describes the
+ * fixed grid (seq_count, n_head, ceil(max_seq_len / block_m)) that this call
+ * does not use): work items are only the real Q tiles of every sample
+ * (times Hq heads), ordered by the number of blocks they must compute and
+ * pulled by a persistent grid of one CTA per SM.
+ *
+ *   q                 device bf16 [T][Hq][D], contiguous, 16-byte aligned.
+ *   k, v              device bf16 [T][Hkv][D], contiguous, 16-byte aligned.
+ *   n_heads_q         Hq >= 1;  n_heads_kv: Hkv >= 1 with Hq % Hkv == 0.
+ *   head_dim          64 or 128.
+ *   cu_seqlens        device int32[n_seqs + 1], n_seqs >= 1.
+ *   startend_row_indices  device int32[n_mask_heads][4][T] (LTS, LTE, UTS,
+ *                     UTE) or NULL for no interval mask (then n_mask_heads
+ *                     is ignored and block_minmax must be NULL).
+ *   n_mask_heads      1 (shared by every head) or Hq (mask head h for q head h).
+ *   block_minmax      device output of fm_mask_block_minmax with the same
+ *                     cu_seqlens, startend_row_indices and block_n.
+ *   causal            nonzero: the whole upper triangle is masked.
+ *   softmax_scale     > 0, or 0 for 1/sqrt(head_dim).
+ *   block_m, block_n  Q / KV tile sizes, each 64 or 128.
+ *   out               device bf16 [T][Hq][D], 16-byte aligned (written).
+ *   lse               device float [Hq][T] (written).
+ *   block_class_counts  optional device int64[3]; when not NULL, the counts
+ *                     of fully masked, partially masked and unmasked blocks
+ *                     over all (sample, Q tile, KV tile, q head) are ADDED
+ *                     to it.
+ *   workspace         device buffer of workspace_bytes >=
+ *                     fm_attn_fwd_workspace_size(T, n_seqs, Hq, block_m),
+ *                     256-byte aligned; its contents need no initialisation
+ *                     and are overwritten.  Calls that share a workspace must
+ *                     be ordered on one stream.
+ *   flags             FM_FLAG_FORCE_INT64 or 0.
+ */
+FM_API fm_status fm_attn_fwd_varlen(const void* q, const void* k, const void* v, int64_t total_tokens,
+                             int n_heads_q, int n_heads_kv, int head_dim,
+                             const int32_t* cu_seqlens, int n_seqs,
+                             const int32_t* startend_row_indices, int n_mask_heads,
+                             const int32_t* block_minmax, int causal, float softmax_scale,
+                             int block_m, int block_n, void* out, float* lse,
+                             int64_t* block_class_counts, void* workspace,
+                             size_t workspace_bytes, uint32_t flags, void* stream);
+
+/*
+ * fm_attn_fwd_num_work_items -- after fm_attn_fwd_varlen has completed on
+ * `stream`, copies to *host_items the number of work items its scheduler
+ * built (real Q tiles times Hq).  Synchronises `stream`.
+ */
+FM_API fm_status fm_attn_fwd_num_work_items(const void* workspace, int64_t* host_items, void* stream);
+
+/*
+ * fm_get_device_error -- synchronises `stream` and copies the device error
+ * word of the last fm_attn_fwd_varlen that used `workspace` into *host_err
+ * (a bit set of FM_DEVERR_*; 0 when clean).
+ */
+FM_API fm_status fm_get_device_error(const void* workspace, int32_t* host_err, void* stream);
+
+/*
+ * fm_debug_bounded_wait -- runs the pipeline's bounded mbarrier wait once on
+ * a barrier that nothing ever arrives at, with a limit of timeout_ns, and
+ * writes the resulting status (FM_ERR_TIMEOUT when the limit expired) to
+ * device int32 *device_status.  Used to check the timeout path without
+ * hanging a GPU.  timeout_ns must be in (0, 10^9].
+ */
+FM_API fm_status fm_debug_bounded_wait(int32_t* device_status, uint64_t timeout_ns, void* stream);
+
+/* Human-readable name of a status code. */
+FM_API const char* fm_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+FM_API int fm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FM_H_ */

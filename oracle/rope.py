@@ -41,11 +41,19 @@ def rotate_half(x: np.ndarray) -> np.ndarray:
 
 
 def rope_apply(x: np.ndarray, cu_seqlens: np.ndarray, theta: float,
-               backward: bool = False) -> np.ndarray:
-    """Rotate ``x`` of shape [T, H, D] (float64); ``backward`` flips sin."""
+               backward: bool = False, tokens=None) -> np.ndarray:
+    """Rotate ``x`` of shape [T, H, D] (float64); ``backward`` flips sin.
+
+    With ``tokens`` (global token indices), ``x`` holds only those tokens'
+    rows, [len(tokens), H, D], and each row keeps its own position.
+    """
     x = np.asarray(x, dtype=np.float64)
-    T, _, D = x.shape
-    ang = positions(cu_seqlens, T)[:, None].astype(np.float64) * frequencies(D, theta)[None, :]
+    _, _, D = x.shape
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    pos = positions(cu, int(cu[-1]))
+    if tokens is not None:
+        pos = pos[np.asarray(tokens, dtype=np.int64)]
+    ang = pos[:, None].astype(np.float64) * frequencies(D, theta)[None, :]
     cos = np.cos(ang)
     sin = np.sin(ang)
     if backward:

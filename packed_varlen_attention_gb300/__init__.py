@@ -1,0 +1,239 @@
+"""Python binding of libfm (packed variable-length FlashMask attention, GB300).
+
+Argument marshalling only: every step runs in the CUDA kernels of
+``libfm.so`` (built in place by ``packed_varlen_attention_gb300.build``).
+PyTorch supplies device memory and the current stream.  There is no CPU
+fallback: if the library is missing or the device is not sm_103, every call
+raises.
+
+Entry points (same names as the C ABI in ``include/fm.h``):
+
+* ``rope_qk_varlen``       fused in-place QK RoPE, positions reset per sample
+* ``mask_block_minmax``    FlashMask per-key-tile min/max of LTS/LTE/UTS/UTE
+* ``attn_fwd_varlen``      FlashMask attention forward (out, lse)
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = [
+    "FMError",
+    "rope_qk_varlen",
+    "num_kv_tiles_bound",
+    "mask_block_minmax",
+    "attn_fwd_workspace_size",
+    "attn_fwd_varlen",
+    "attn_fwd_num_work_items",
+    "get_device_error",
+    "debug_bounded_wait",
+    "status_string",
+    "version",
+    "library_path",
+    "EXPORTED_SYMBOLS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libfm.so")
+_LIB = None
+
+FM_FLAG_FORCE_INT64 = 0x1
+FM_DEVERR_TIMEOUT = 0x1
+FM_DEVERR_DATA = 0x2
+
+_c_i64 = ctypes.c_int64
+_c_int = ctypes.c_int
+_c_u32 = ctypes.c_uint32
+_c_vp = ctypes.c_void_p
+
+_SIGNATURES = {
+    "fm_rope_qk_varlen": (_c_int, [_c_vp, _c_vp, _c_i64, _c_int, _c_int, _c_int, _c_i64, _c_i64,
+                                   _c_vp, _c_int, ctypes.c_double, _c_int, _c_u32, _c_vp]),
+    "fm_num_kv_tiles_bound": (_c_i64, [_c_i64, _c_int, _c_int]),
+    "fm_mask_block_minmax": (_c_int, [_c_vp, _c_int, _c_i64, _c_vp, _c_int, _c_int, _c_vp,
+                                      _c_i64, _c_vp]),
+    "fm_attn_fwd_workspace_size": (ctypes.c_size_t, [_c_i64, _c_int, _c_int, _c_int]),
+    "fm_attn_fwd_varlen": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_int, _c_int, _c_int, _c_vp,
+                                    _c_int, _c_vp, _c_int, _c_vp, _c_int, ctypes.c_float, _c_int,
+                                    _c_int, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_u32,
+                                    _c_vp]),
+    "fm_attn_fwd_num_work_items": (_c_int, [_c_vp, ctypes.POINTER(_c_i64), _c_vp]),
+    "fm_get_device_error": (_c_int, [_c_vp, ctypes.POINTER(ctypes.c_int32), _c_vp]),
+    "fm_debug_bounded_wait": (_c_int, [_c_vp, ctypes.c_uint64, _c_vp]),
+    "fm_status_string": (ctypes.c_char_p, [_c_int]),
+    "fm_version": (_c_int, []),
+}
+EXPORTED_SYMBOLS = tuple(_SIGNATURES)
+
+
+class FMError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {status_string(code)} ({code})")
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                "libfm.so is not built; run `python -m packed_varlen_attention_gb300.build`")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def status_string(code: int) -> str:
+    return _lib().fm_status_string(int(code)).decode()
+
+
+def version() -> int:
+    return int(_lib().fm_version())
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise FMError(fn, code)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def rope_qk_varlen(q: torch.Tensor, k: Optional[torch.Tensor], cu_seqlens: torch.Tensor,
+                   theta: float, backward: bool = False, force_int64: bool = False,
+                   stream=None) -> None:
+    """Rotate q [T, Hq, D] and k [T, Hkv, D] (bf16, CUDA) in place."""
+    _need(q, "q", torch.bfloat16)
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    T, hq, d = q.shape
+    if q.stride(2) != 1 or q.stride(1) != d:
+        raise ValueError("q must have contiguous heads ([T, H, D] with stride (s, D, 1))")
+    hkv, ks = 0, 0
+    if k is not None:
+        _need(k, "k", torch.bfloat16)
+        if k.shape[0] != T or k.shape[2] != d or k.stride(2) != 1 or k.stride(1) != d:
+            raise ValueError("k must be [T, Hkv, D] with contiguous heads")
+        hkv, ks = k.shape[1], k.stride(0)
+    _check("fm_rope_qk_varlen", _lib().fm_rope_qk_varlen(
+        _ptr(q), _ptr(k), T, hq, hkv, d, q.stride(0), ks, _ptr(cu_seqlens),
+        cu_seqlens.numel() - 1, float(theta), int(bool(backward)),
+        FM_FLAG_FORCE_INT64 if force_int64 else 0, _stream(stream)))
+
+
+def num_kv_tiles_bound(total_tokens: int, n_seqs: int, block_n: int) -> int:
+    return int(_lib().fm_num_kv_tiles_bound(total_tokens, n_seqs, block_n))
+
+
+def mask_block_minmax(startend_row_indices: torch.Tensor, cu_seqlens: torch.Tensor,
+                      block_n: int, out: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
+    """Per-key-tile statistics int32 [Hm, 8, n_slots] of the column intervals."""
+    _need(startend_row_indices, "startend_row_indices", torch.int32)
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    sri = startend_row_indices
+    if sri.dim() != 3 or sri.shape[1] != 4 or not sri.is_contiguous():
+        raise ValueError("startend_row_indices must be contiguous int32 [Hm, 4, T]")
+    hm, _, T = sri.shape
+    n_seqs = cu_seqlens.numel() - 1
+    n_slots = num_kv_tiles_bound(T, n_seqs, block_n)
+    if out is None:
+        out = torch.empty((hm, 8, n_slots), dtype=torch.int32, device=sri.device)
+    _need(out, "out", torch.int32)
+    _check("fm_mask_block_minmax", _lib().fm_mask_block_minmax(
+        _ptr(sri), hm, T, _ptr(cu_seqlens), n_seqs, block_n, _ptr(out), out.numel(),
+        _stream(stream)))
+    return out
+
+
+def attn_fwd_workspace_size(total_tokens: int, n_seqs: int, n_heads_q: int, block_m: int) -> int:
+    return int(_lib().fm_attn_fwd_workspace_size(total_tokens, n_seqs, n_heads_q, block_m))
+
+
+def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
+                    startend_row_indices: Optional[torch.Tensor] = None,
+                    block_minmax: Optional[torch.Tensor] = None, causal: bool = False,
+                    softmax_scale: float = 0.0, block_m: int = 128, block_n: int = 128,
+                    out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                    class_counts: Optional[torch.Tensor] = None,
+                    workspace: Optional[torch.Tensor] = None, force_int64: bool = False,
+                    stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """FlashMask attention forward. Returns (out [T, Hq, D] bf16, lse [Hq, T] fp32)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous [T, H, D]")
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    T, hq, d = q.shape
+    hkv = k.shape[1]
+    n_seqs = cu_seqlens.numel() - 1
+    hm = 0
+    if startend_row_indices is not None:
+        _need(startend_row_indices, "startend_row_indices", torch.int32)
+        hm = startend_row_indices.shape[0]
+        if block_minmax is None:
+            raise ValueError("block_minmax (from mask_block_minmax) is required with a mask")
+        _need(block_minmax, "block_minmax", torch.int32)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((hq, T), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        nbytes = attn_fwd_workspace_size(T, n_seqs, hq, block_m)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if class_counts is not None:
+        _need(class_counts, "class_counts", torch.int64)
+    _check("fm_attn_fwd_varlen", _lib().fm_attn_fwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), T, hq, hkv, d, _ptr(cu_seqlens), n_seqs,
+        _ptr(startend_row_indices), hm, _ptr(block_minmax), int(bool(causal)),
+        float(softmax_scale), block_m, block_n, _ptr(out), _ptr(lse), _ptr(class_counts),
+        _ptr(workspace), workspace.numel(), FM_FLAG_FORCE_INT64 if force_int64 else 0,
+        _stream(stream)))
+    return out, lse
+
+
+def attn_fwd_num_work_items(workspace: torch.Tensor, stream=None) -> int:
+    n = _c_i64(0)
+    _check("fm_attn_fwd_num_work_items",
+           _lib().fm_attn_fwd_num_work_items(_ptr(workspace), ctypes.byref(n), _stream(stream)))
+    return int(n.value)
+
+
+def get_device_error(workspace: torch.Tensor, stream=None) -> int:
+    e = ctypes.c_int32(0)
+    _check("fm_get_device_error",
+           _lib().fm_get_device_error(_ptr(workspace), ctypes.byref(e), _stream(stream)))
+    return int(e.value)
+
+
+def debug_bounded_wait(timeout_ns: int, stream=None) -> int:
+    """Runs one bounded wait on a barrier nothing arrives at; returns its status."""
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    _check("fm_debug_bounded_wait",
+           _lib().fm_debug_bounded_wait(_ptr(status), int(timeout_ns), _stream(stream)))
+    return int(status.item())

@@ -1,0 +1,293 @@
+// fm_api.cu -- the C ABI: argument validation, TMA descriptor encoding and
+// kernel launches.  Nothing here allocates device memory or synchronises,
+// except the two documented read-back helpers.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fm_internal.h"
+
+namespace {
+
+using fm::AttnParams;
+
+constexpr int kMaxDevices = 64;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+struct DeviceInfo {
+  bool known = false;
+  bool supported = false;
+  int num_sms = 0;
+};
+
+// Current device must be sm_103 (GB300); SM count cached per device.
+fm_status device_info(int* num_sms) {
+  static DeviceInfo info[kMaxDevices];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FM_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FM_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceInfo& d = info[dev];
+  if (!d.known) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FM_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3);
+    d.num_sms = sms;
+    d.known = true;
+  }
+  if (!d.supported) return FM_ERR_UNSUPPORTED;
+  if (num_sms) *num_sms = d.num_sms;
+  return FM_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+fm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FM_OK : FM_ERR_CUDA; }
+
+// 2-D bf16 tensor map over [rows][cols] (cols contiguous) with a
+// 64-column x box_rows box and 128-byte swizzle; out-of-range rows read 0.
+bool make_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+              uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fm_version(void) { return 100; }
+
+const char* fm_status_string(int status) {
+  switch (status) {
+    case FM_OK: return "FM_OK";
+    case FM_ERR_INVALID_ARG: return "FM_ERR_INVALID_ARG";
+    case FM_ERR_UNSUPPORTED: return "FM_ERR_UNSUPPORTED";
+    case FM_ERR_ALIGNMENT: return "FM_ERR_ALIGNMENT";
+    case FM_ERR_WORKSPACE: return "FM_ERR_WORKSPACE";
+    case FM_ERR_CUDA: return "FM_ERR_CUDA";
+    case FM_ERR_TIMEOUT: return "FM_ERR_TIMEOUT";
+    case FM_ERR_DEVICE_DATA: return "FM_ERR_DEVICE_DATA";
+    default: return "FM_ERR_UNKNOWN";
+  }
+}
+
+fm_status fm_rope_qk_varlen(void* q, void* k, int64_t total_tokens, int n_heads_q,
+                            int n_heads_kv, int head_dim, int64_t q_token_stride,
+                            int64_t k_token_stride, const int32_t* cu_seqlens, int n_seqs,
+                            double theta, int backward, uint32_t flags, void* stream) {
+  if (total_tokens < 0 || n_heads_q < 1 || n_heads_kv < 0 || n_seqs < 1) return FM_ERR_INVALID_ARG;
+  if (q == nullptr || cu_seqlens == nullptr || (n_heads_kv > 0 && k == nullptr))
+    return FM_ERR_INVALID_ARG;
+  if (!(theta > 0.0) || !std::isfinite(theta)) return FM_ERR_INVALID_ARG;
+  if (flags & ~FM_FLAG_FORCE_INT64) return FM_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return FM_ERR_UNSUPPORTED;
+  if (q_token_stride < static_cast<int64_t>(n_heads_q) * head_dim) return FM_ERR_INVALID_ARG;
+  if (n_heads_kv > 0 && k_token_stride < static_cast<int64_t>(n_heads_kv) * head_dim)
+    return FM_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || q_token_stride % 8 != 0) return FM_ERR_ALIGNMENT;
+  if (n_heads_kv > 0 && (!aligned(k, 16) || k_token_stride % 8 != 0)) return FM_ERR_ALIGNMENT;
+  if (n_heads_q + n_heads_kv > 8 * 65535) return FM_ERR_UNSUPPORTED;
+  if (total_tokens == 0) return FM_OK;
+  fm_status st = device_info(nullptr);
+  if (st != FM_OK) return st;
+
+  fm::RopeFreqs fr;
+  std::memset(&fr, 0, sizeof(fr));
+  for (int i = 0; i < head_dim / 2; ++i) {
+    const double f = std::pow(theta, -2.0 * i / head_dim);
+    fr.hi[i] = static_cast<float>(f);
+    fr.lo[i] = static_cast<float>(f - static_cast<double>(fr.hi[i]));
+  }
+  const int64_t lim = int64_t(1) << 31;
+  bool use64 = (flags & FM_FLAG_FORCE_INT64) != 0;
+  use64 = use64 || total_tokens * q_token_stride >= lim;
+  use64 = use64 || (n_heads_kv > 0 && total_tokens * k_token_stride >= lim);
+  use64 = use64 || total_tokens * (head_dim / 16) >= lim;
+  return from_cuda(fm::launch_rope(q, k, total_tokens, n_heads_q, n_heads_kv, head_dim,
+                                   q_token_stride, k_token_stride, cu_seqlens, n_seqs, fr,
+                                   backward != 0, use64, static_cast<cudaStream_t>(stream)));
+}
+
+int64_t fm_num_kv_tiles_bound(int64_t total_tokens, int n_seqs, int block_n) {
+  if (total_tokens < 0 || n_seqs < 0 || block_n <= 0) return -1;
+  return total_tokens / block_n + n_seqs;
+}
+
+fm_status fm_mask_block_minmax(const int32_t* startend_row_indices, int n_mask_heads,
+                               int64_t total_tokens, const int32_t* cu_seqlens, int n_seqs,
+                               int block_n, int32_t* block_minmax,
+                               int64_t block_minmax_capacity, void* stream) {
+  if (startend_row_indices == nullptr || cu_seqlens == nullptr || block_minmax == nullptr)
+    return FM_ERR_INVALID_ARG;
+  if (n_mask_heads < 1 || n_seqs < 1 || total_tokens < 0 || total_tokens > INT32_MAX)
+    return FM_ERR_INVALID_ARG;
+  if (block_n != 64 && block_n != 128) return FM_ERR_UNSUPPORTED;
+  const int64_t n_slots = fm_num_kv_tiles_bound(total_tokens, n_seqs, block_n);
+  if (block_minmax_capacity < n_slots * 8 * n_mask_heads) return FM_ERR_WORKSPACE;
+  if (!aligned(startend_row_indices, 4) || !aligned(block_minmax, 4)) return FM_ERR_ALIGNMENT;
+  fm_status st = device_info(nullptr);
+  if (st != FM_OK) return st;
+  return from_cuda(fm::launch_mask_minmax(startend_row_indices, n_mask_heads, total_tokens,
+                                          cu_seqlens, n_seqs, block_n, block_minmax, n_slots,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+size_t fm_attn_fwd_workspace_size(int64_t total_tokens, int n_seqs, int n_heads_q, int block_m) {
+  if (total_tokens < 0 || n_seqs < 0 || n_heads_q < 1 || (block_m != 64 && block_m != 128))
+    return 0;
+  return fm::attn_workspace_bytes(total_tokens, n_seqs, block_m);
+}
+
+fm_status fm_attn_fwd_varlen(const void* q, const void* k, const void* v, int64_t total_tokens,
+                             int n_heads_q, int n_heads_kv, int head_dim,
+                             const int32_t* cu_seqlens, int n_seqs,
+                             const int32_t* startend_row_indices, int n_mask_heads,
+                             const int32_t* block_minmax, int causal, float softmax_scale,
+                             int block_m, int block_n, void* out, float* lse,
+                             int64_t* block_class_counts, void* workspace,
+                             size_t workspace_bytes, uint32_t flags, void* stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || lse == nullptr ||
+      cu_seqlens == nullptr || workspace == nullptr)
+    return FM_ERR_INVALID_ARG;
+  if (total_tokens < 0 || total_tokens > INT32_MAX - 256 || n_seqs < 1) return FM_ERR_INVALID_ARG;
+  if (n_heads_q < 1 || n_heads_kv < 1 || n_heads_q % n_heads_kv != 0) return FM_ERR_INVALID_ARG;
+  if (flags & ~FM_FLAG_FORCE_INT64) return FM_ERR_INVALID_ARG;
+  if (startend_row_indices != nullptr) {
+    if (n_mask_heads != 1 && n_mask_heads != n_heads_q) return FM_ERR_INVALID_ARG;
+    if (block_minmax == nullptr) return FM_ERR_INVALID_ARG;
+  } else {
+    if (block_minmax != nullptr) return FM_ERR_INVALID_ARG;
+    n_mask_heads = 0;
+  }
+  if (!(softmax_scale >= 0.0f) || !std::isfinite(softmax_scale)) return FM_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return FM_ERR_UNSUPPORTED;
+  if ((block_m != 64 && block_m != 128) || (block_n != 64 && block_n != 128))
+    return FM_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(workspace, 256))
+    return FM_ERR_ALIGNMENT;
+  if (block_class_counts != nullptr && !aligned(block_class_counts, 8)) return FM_ERR_ALIGNMENT;
+  if (workspace_bytes < fm::attn_workspace_bytes(total_tokens, n_seqs, block_m))
+    return FM_ERR_WORKSPACE;
+  const int64_t n_qslots = total_tokens / block_m + n_seqs;
+  if (n_qslots * n_heads_q >= (int64_t(1) << 31)) return FM_ERR_UNSUPPORTED;
+  if (total_tokens == 0) return FM_OK;
+  int num_sms = 0;
+  fm_status st = device_info(&num_sms);
+  if (st != FM_OK) return st;
+
+  CUtensorMap tq, tk, tv;
+  const uint64_t T = static_cast<uint64_t>(total_tokens);
+  if (!make_map(&tq, q, static_cast<uint64_t>(n_heads_q) * head_dim, T, 128) ||
+      !make_map(&tk, k, static_cast<uint64_t>(n_heads_kv) * head_dim, T, block_n) ||
+      !make_map(&tv, v, static_cast<uint64_t>(n_heads_kv) * head_dim, T, block_n))
+    return FM_ERR_CUDA;
+
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.lse = lse;
+  p.cu = cu_seqlens;
+  p.sri = startend_row_indices;
+  p.minmax = block_minmax;
+  p.class_counts = block_class_counts;
+  p.ws = reinterpret_cast<fm::AttnWorkspaceHeader*>(ws);
+  p.hist = reinterpret_cast<int*>(ws + sizeof(fm::AttnWorkspaceHeader));
+  uint8_t* tail = ws + sizeof(fm::AttnWorkspaceHeader) + fm::kCostBins * sizeof(int);
+  p.slot_info = reinterpret_cast<int2*>(tail);
+  p.order = reinterpret_cast<int2*>(tail + n_qslots * sizeof(int2));
+  p.cost = reinterpret_cast<int*>(tail + 2 * n_qslots * sizeof(int2));
+  p.T = total_tokens;
+  p.n_qslots = n_qslots;
+  p.n_kv_slots = fm_num_kv_tiles_bound(total_tokens, n_seqs, block_n);
+  p.n_seqs = n_seqs;
+  p.hq = n_heads_q;
+  p.hkv = n_heads_kv;
+  p.hm = n_mask_heads;
+  p.head_dim = head_dim;
+  p.block_m = block_m;
+  p.block_n = block_n;
+  p.causal = causal != 0;
+  const double scale = softmax_scale > 0.0f ? softmax_scale : 1.0 / std::sqrt(double(head_dim));
+  p.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
+  p.timeout_ns = 1000000000ull;
+
+  const int64_t lim = int64_t(1) << 31;
+  const bool use64 = (flags & FM_FLAG_FORCE_INT64) != 0 ||
+                     total_tokens * n_heads_q * head_dim >= lim ||
+                     total_tokens * n_heads_kv * head_dim >= lim;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t clear = sizeof(fm::AttnWorkspaceHeader) + fm::kCostBins * sizeof(int);
+  if (cudaMemsetAsync(workspace, 0, clear, s) != cudaSuccess) return FM_ERR_CUDA;
+  return from_cuda(fm::launch_attn_fwd(p, tq, tk, tv, use64, num_sms, s));
+}
+
+fm_status fm_attn_fwd_num_work_items(const void* workspace, int64_t* host_items, void* stream) {
+  if (workspace == nullptr || host_items == nullptr) return FM_ERR_INVALID_ARG;
+  const auto* hdr = static_cast<const fm::AttnWorkspaceHeader*>(workspace);
+  int32_t n = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&n, &hdr->n_items, sizeof(n), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return FM_ERR_CUDA;
+  *host_items = n;
+  return FM_OK;
+}
+
+fm_status fm_get_device_error(const void* workspace, int32_t* host_err, void* stream) {
+  if (workspace == nullptr || host_err == nullptr) return FM_ERR_INVALID_ARG;
+  const auto* hdr = static_cast<const fm::AttnWorkspaceHeader*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(host_err, &hdr->error_word, sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return FM_ERR_CUDA;
+  return FM_OK;
+}
+
+fm_status fm_debug_bounded_wait(int32_t* device_status, uint64_t timeout_ns, void* stream) {
+  if (device_status == nullptr || timeout_ns == 0 || timeout_ns > 1000000000ull)
+    return FM_ERR_INVALID_ARG;
+  fm_status st = device_info(nullptr);
+  if (st != FM_OK) return st;
+  return from_cuda(
+      fm::launch_bounded_wait_probe(device_status, timeout_ns, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,77 @@
+// fm_internal.h -- launchers shared between the C ABI (fm_api.cu) and the
+// kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fm.h"
+
+namespace fm {
+
+constexpr int kMaxHalfDim = 64;  // head_dim <= 128
+
+// Inverse RoPE frequencies theta^(-2i/D) as double-float pairs (hi + lo).
+struct RopeFreqs {
+  float hi[kMaxHalfDim];
+  float lo[kMaxHalfDim];
+};
+
+cudaError_t launch_rope(void* q, void* k, int64_t T, int hq, int hkv, int head_dim,
+                        int64_t q_stride, int64_t k_stride, const int32_t* cu, int n_seqs,
+                        const RopeFreqs& freqs, bool backward, bool use_int64,
+                        cudaStream_t stream);
+
+cudaError_t launch_mask_minmax(const int32_t* sri, int n_mask_heads, int64_t T,
+                               const int32_t* cu, int n_seqs, int block_n, int32_t* out,
+                               int64_t n_slots, cudaStream_t stream);
+
+// Workspace header of the attention forward pass.
+struct AttnWorkspaceHeader {
+  uint32_t work_counter;  // next work item (atomic)
+  int32_t n_qtiles;       // real Q tiles found by the planner
+  int32_t n_items;        // n_qtiles * Hq
+  int32_t error_word;     // FM_DEVERR_* bits
+  int32_t pad[60];
+};
+static_assert(sizeof(AttnWorkspaceHeader) == 256, "header is 256 bytes");
+
+constexpr int kCostBins = 1024;  // scheduler histogram bins (cost = non-F KV tiles)
+
+struct AttnParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  float* lse;
+  const int32_t* cu;
+  const int32_t* sri;
+  const int32_t* minmax;
+  int64_t* class_counts;
+  AttnWorkspaceHeader* ws;
+  int* cost;         // [n_qslots]
+  int2* slot_info;   // [n_qslots] (sample, q tile)
+  int2* order;       // [n_qslots] work order (sample, q tile)
+  int* hist;         // [kCostBins]
+  int64_t T;
+  int64_t n_qslots;
+  int64_t n_kv_slots;
+  int n_seqs;
+  int hq, hkv, hm;
+  int head_dim;
+  int block_m, block_n;
+  int causal;
+  float scale_log2;
+  uint64_t timeout_ns;
+};
+
+size_t attn_workspace_bytes(int64_t T, int n_seqs, int block_m);
+
+cudaError_t launch_attn_fwd(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, bool use_int64, int num_sms,
+                            cudaStream_t stream);
+
+cudaError_t launch_bounded_wait_probe(int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace fm

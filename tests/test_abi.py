@@ -1,0 +1,103 @@
+"""The C ABI library: it loads, exports every declared symbol, and its
+host-side logic (validation, sizes) answers without touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from helpers import ROOT, ensure_library
+
+
+@pytest.fixture(scope="module")
+def fm():
+    return ensure_library()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "fm.h")).read()
+    return sorted(set(re.findall(r"FM_API[^;(]*?\b(fm_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_hot_path_calls():
+    names = _declared()
+    for n in ("fm_rope_qk_varlen", "fm_mask_block_minmax", "fm_attn_fwd_varlen"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(fm):
+    lib = ctypes.CDLL(fm.library_path())
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert sorted(fm.EXPORTED_SYMBOLS) == _declared()
+
+
+def test_status_strings_and_version(fm):
+    assert fm.version() >= 100
+    assert fm.status_string(0) == "FM_OK"
+    assert fm.status_string(6) == "FM_ERR_TIMEOUT"
+    assert fm.status_string(99) == "FM_ERR_UNKNOWN"
+
+
+def test_kv_tile_bound_and_slot_layout(fm):
+    assert fm.num_kv_tiles_bound(256, 3, 64) == 4 + 3
+    assert fm.num_kv_tiles_bound(-1, 3, 64) == -1
+    rng = np.random.default_rng(0)
+    for _ in range(50):
+        lens = rng.integers(0, 700, size=rng.integers(1, 12))
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+        T = int(cu[-1])
+        for bn in (64, 128):
+            bound = fm.num_kv_tiles_bound(T, len(lens), bn)
+            used = set()
+            for s, n in enumerate(lens):
+                for j in range(-(-int(n) // bn)):
+                    slot = int(cu[s]) // bn + s + j
+                    assert 0 <= slot < bound and slot not in used
+                    used.add(slot)
+
+
+def test_workspace_size(fm):
+    a = fm.attn_fwd_workspace_size(8192, 30, 32, 128)
+    b = fm.attn_fwd_workspace_size(8192, 30, 32, 64)
+    assert a > 0 and b > a and a % 256 == 0
+    assert fm.attn_fwd_workspace_size(10, 1, 1, 96) == 0
+
+
+def _raw(fm):
+    return fm._lib()
+
+
+def test_validation_rejects_before_any_launch(fm):
+    lib = _raw(fm)
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    # unsupported head_dim
+    assert lib.fm_rope_qk_varlen(fake, fake, 16, 1, 1, 96, 96, 96, fake, 1, 1e4, 0, 0, None) == 2
+    # null q
+    assert lib.fm_rope_qk_varlen(None, fake, 16, 1, 1, 64, 64, 64, fake, 1, 1e4, 0, 0, None) == 1
+    # misaligned q
+    assert lib.fm_rope_qk_varlen(ctypes.c_void_p(0x10002), fake, 16, 1, 1, 64, 64, 64, fake, 1,
+                                 1e4, 0, 0, None) == 3
+    # bad theta, unknown flag
+    assert lib.fm_rope_qk_varlen(fake, fake, 16, 1, 1, 64, 64, 64, fake, 1, -1.0, 0, 0, None) == 1
+    assert lib.fm_rope_qk_varlen(fake, fake, 16, 1, 1, 64, 64, 64, fake, 1, 1e4, 0, 8, None) == 1
+    # minmax: capacity too small, bad block size
+    assert lib.fm_mask_block_minmax(fake, 1, 256, fake, 3, 64, fake, 10, None) == 4
+    assert lib.fm_mask_block_minmax(fake, 1, 256, fake, 3, 96, fake, 10 ** 6, None) == 2
+    # attention: GQA ratio, mask heads, block sizes, workspace, alignment
+    def attn(hq=4, hkv=2, d=128, sri=None, hm=0, mm=None, bm=128, bn=128, ws_bytes=1 << 20,
+             ws=fake, out=fake):
+        return lib.fm_attn_fwd_varlen(fake, fake, fake, 256, hq, hkv, d, fake, 2, sri, hm, mm, 1,
+                                      0.0, bm, bn, out, fake, None, ws, ws_bytes, 0, None)
+    assert attn(hq=3, hkv=2) == 1
+    assert attn(sri=fake, hm=2, mm=fake) == 1
+    assert attn(sri=fake, hm=1, mm=None) == 1
+    assert attn(sri=None, mm=fake) == 1
+    assert attn(d=96) == 2
+    assert attn(bm=32) == 2
+    assert attn(ws_bytes=16) == 4
+    assert attn(ws=ctypes.c_void_p(0x10010)) == 3
+    assert attn(out=ctypes.c_void_p(0x10008)) == 3
+    assert lib.fm_debug_bounded_wait(fake, 0, None) == 1
