@@ -201,6 +201,36 @@ FM_API fm_status fm_attn_fwd_varlen(const void* q, const void* k, const void* v,
                              size_t workspace_bytes, uint32_t flags, void* stream);
 
 /*
+ * fm_attn_fwd_varlen_noalloc -- fm_attn_fwd_varlen for callers that cannot
+ * allocate device memory.  The pages have no counterpart: this entry point
+ * exists for integration only.
+ *
+ * Same arguments and results as fm_attn_fwd_varlen, without workspace and
+ * workspace_bytes.  Callers without an allocator handle (a plugin that only
+ * receives its input and output buffers), callers whose device memory is
+ * owned by a framework's caching allocator, and latency-critical paths that
+ * must not call cudaMalloc (it may synchronise the device) can use it: the
+ * scheduler scratch lives in a fixed array inside the library (a little
+ * under 0.7 MB, held by every GPU that loads the library until the process
+ * exits).  Limit: floor(T / block_m) + n_seqs <= 32768 Q-tile slots, else
+ * FM_ERR_WORKSPACE is returned before any launch.  The first call on a
+ * device resolves the array's device address (with that device current);
+ * make that first call before any stream capture.  All calls on a device
+ * share the array and each call clears what must start at zero; calls that
+ * overlap on the GPU race on it, so order them on one stream.  Nothing is
+ * allocated or freed.
+ */
+FM_API fm_status fm_attn_fwd_varlen_noalloc(const void* q, const void* k, const void* v,
+                                            int64_t total_tokens, int n_heads_q, int n_heads_kv,
+                                            int head_dim, const int32_t* cu_seqlens, int n_seqs,
+                                            const int32_t* startend_row_indices,
+                                            int n_mask_heads, const int32_t* block_minmax,
+                                            int causal, float softmax_scale, int block_m,
+                                            int block_n, void* out, float* lse,
+                                            int64_t* block_class_counts, uint32_t flags,
+                                            void* stream);
+
+/*
  * fm_attn_fwd_num_work_items -- after fm_attn_fwd_varlen has completed on
  * `stream`, copies to *host_items the number of work items its scheduler
  * built (real Q tiles times Hq).  Synchronises `stream`.

@@ -28,6 +28,7 @@ __all__ = [
     "mask_block_minmax",
     "attn_fwd_workspace_size",
     "attn_fwd_varlen",
+    "attn_fwd_varlen_noalloc",
     "attn_fwd_num_work_items",
     "get_device_error",
     "debug_bounded_wait",
@@ -61,6 +62,10 @@ _SIGNATURES = {
                                     _c_int, _c_vp, _c_int, _c_vp, _c_int, ctypes.c_float, _c_int,
                                     _c_int, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_u32,
                                     _c_vp]),
+    "fm_attn_fwd_varlen_noalloc": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_int, _c_int, _c_int,
+                                            _c_vp, _c_int, _c_vp, _c_int, _c_vp, _c_int,
+                                            ctypes.c_float, _c_int, _c_int, _c_vp, _c_vp, _c_vp,
+                                            _c_u32, _c_vp]),
     "fm_attn_fwd_num_work_items": (_c_int, [_c_vp, ctypes.POINTER(_c_i64), _c_vp]),
     "fm_get_device_error": (_c_int, [_c_vp, ctypes.POINTER(ctypes.c_int32), _c_vp]),
     "fm_debug_bounded_wait": (_c_int, [_c_vp, ctypes.c_uint64, _c_vp]),
@@ -214,6 +219,51 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
         float(softmax_scale), block_m, block_n, _ptr(out), _ptr(lse), _ptr(class_counts),
         _ptr(workspace), workspace.numel(), FM_FLAG_FORCE_INT64 if force_int64 else 0,
         _stream(stream)))
+    return out, lse
+
+
+def attn_fwd_varlen_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                            cu_seqlens: torch.Tensor,
+                            startend_row_indices: Optional[torch.Tensor] = None,
+                            block_minmax: Optional[torch.Tensor] = None, causal: bool = False,
+                            softmax_scale: float = 0.0, block_m: int = 128, block_n: int = 128,
+                            out: Optional[torch.Tensor] = None,
+                            lse: Optional[torch.Tensor] = None,
+                            class_counts: Optional[torch.Tensor] = None,
+                            force_int64: bool = False,
+                            stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """``attn_fwd_varlen`` for callers that cannot allocate device memory.
+
+    The library keeps the scheduler scratch in a fixed device array of its own
+    (limit: T // block_m + n_seqs <= 32768), so no workspace is passed.  Pass
+    ``out`` and ``lse`` as well to keep this call free of allocations; the
+    first call on a device should come before any stream capture, and calls
+    must not overlap on the GPU (they share the array).
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous [T, H, D]")
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    T, hq, d = q.shape
+    hm = 0
+    if startend_row_indices is not None:
+        _need(startend_row_indices, "startend_row_indices", torch.int32)
+        hm = startend_row_indices.shape[0]
+        if block_minmax is None:
+            raise ValueError("block_minmax (from mask_block_minmax) is required with a mask")
+        _need(block_minmax, "block_minmax", torch.int32)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((hq, T), dtype=torch.float32, device=q.device)
+    if class_counts is not None:
+        _need(class_counts, "class_counts", torch.int64)
+    _check("fm_attn_fwd_varlen_noalloc", _lib().fm_attn_fwd_varlen_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), T, hq, k.shape[1], d, _ptr(cu_seqlens),
+        cu_seqlens.numel() - 1, _ptr(startend_row_indices), hm, _ptr(block_minmax),
+        int(bool(causal)), float(softmax_scale), block_m, block_n, _ptr(out), _ptr(lse),
+        _ptr(class_counts), FM_FLAG_FORCE_INT64 if force_int64 else 0, _stream(stream)))
     return out, lse
 
 
