@@ -9,30 +9,36 @@
 // the backward operator consumes (section 3.4).
 //
 // How it runs on GB300:
-//   * Planner (two tiny kernels): one warp per sample-local Q tile counts the
-//     blocks that are not fully masked (its cost); a single CTA orders the
-//     real Q tiles by cost, largest first (counting sort over cost bins).
-//     Only real tiles become work items -- not the fixed grid
+//   * Planner (two tiny kernels): one warp per sample-local pair of Q tiles
+//     counts the blocks that are not fully masked (its cost); one CTA orders
+//     the real pairs by cost, largest first (counting sort over cost bins).
+//     Only real tiles become work -- not the fixed grid
 //     (seq_count, n_head, ceil(max_seq_len / Br)) of the Varlen-Packing
 //     technical document, section 2, whose CTAs past a short sample's end do
 //     nothing.
-//   * Persistent main kernel, one CTA per SM, pulling items (Q tile x q head)
-//     from an atomic counter.  Warp roles:
-//       warp 0       producer: classifies the item's KV tiles (warp-parallel,
-//                    32 tiles per step), TMA-loads Q once per item and K/V
-//                    for every non-skipped tile into a 2-stage ring, and
-//                    copies the four mask columns of partially masked tiles;
-//       warp 1       MMA issuer (one thread): S = Q K^T into TMEM (two S
-//                    buffers), then O += P V into a TMEM accumulator, with
-//                    tcgen05.mma kind::f16 (bf16 in, fp32 accumulate);
-//       warps 4..7   softmax: one thread per row of the 128-row tile reads
-//                    its S row from TMEM, applies the mask (partial blocks
-//                    only), keeps the running max / sum, rescales O in TMEM
-//                    only when the max grew by more than 2^8, writes P as
-//                    bf16 into shared memory (128-byte swizzled, K-major),
-//                    and finally normalises O and writes out / lse.
-//     The S MMA of tile j+1 runs on the tensor cores while the softmax
-//     works on tile j.
+//   * Persistent main kernel, one CTA per SM, pulling items (two consecutive
+//     Q tiles of one sample x one q head) from an atomic counter.  The two Q
+//     tiles share every K/V tile the CTA loads.  Warp roles (352 threads):
+//       warp 0      K producer: classifies the item's KV tiles for both Q
+//                   tiles (warp-parallel, 32 tiles per step), publishes
+//                   per-tile metadata (and the mask columns of partially
+//                   masked tiles) in a 4-slot ring, TMA-loads both Q tiles
+//                   once per item and K per tile into a 2-stage ring;
+//       warp 2      V producer: TMA-loads V per tile into a 2-stage ring;
+//       warp 1      MMA issuer (one thread): tcgen05.mma kind::f16, bf16 in,
+//                   fp32 accumulate: S_i = Q_i K^T into TMEM (i = 0, 1), then
+//                   O_i += P_i V with P_i read from TMEM (it overwrites the
+//                   first half of S_i's columns as packed bf16);
+//       warps 3..6  softmax of Q tile 0, warps 7..10 softmax of Q tile 1: one
+//                   thread per tile row (= TMEM lane).  The whole S row is
+//                   loaded from TMEM with one wait, masked (partial blocks
+//                   only), reduced to its max, turned into
+//                   P = 2^(S*scale*log2e - m) with a running sum and stored as
+//                   bf16 into TMEM.  O_i is rescaled in TMEM only when the max
+//                   grew by more than 2^8; the epilogue normalises O_i and
+//                   writes out / lse with guarded stores.
+//     The MMA order per KV tile is PV_0, S_0(next), PV_1, S_1(next): while one
+//     softmax warpgroup works, the tensor cores run the other tile's MMAs.
 //   * Every mbarrier wait is bounded (wall-clock limit) and reports
 //     FM_DEVERR_TIMEOUT in the workspace error word instead of hanging.
 //
@@ -49,55 +55,59 @@
 namespace fm {
 namespace {
 
-constexpr int kThreads = 256;
+// warps 0..2: K producer, MMA issuer, V producer; warps 3..10: softmax (two
+// warpgroups; warp w reads TMEM lanes 32*(w%4)..+31, so each group of four
+// consecutive warps covers all 128 rows).  352 threads leave 184 registers
+// per thread, enough for a whole 128-column S row.
+constexpr int kThreads = 352;
+constexpr int kFirstSoftmaxWarp = 3;
 constexpr int kStages = 2;
 constexpr int kTileM = 128;  // MMA M: TMEM lanes = tile rows
+constexpr int kMetaSlots = 4;
+constexpr int kPrefetchAhead = 3;  // K/V tiles pulled into L2 ahead of their loads
 
-enum : int { kClsF = 0, kClsP = 1, kClsU = 2, kClsStop = 3 };
-enum : int { kFirst = 1, kLast = 2 };
+enum : int { kClsF = 0, kClsP = 1, kClsU = 2 };
+enum : int { kFirst = 1, kLast = 2, kHasQ1 = 4, kStop = 8 };
 
 struct TileMeta {
-  int cls;     // kClsP / kClsU / kClsStop
-  int flags;   // kFirst | kLast
-  int c0, c1;  // key columns [c0, c1)
-  int r0, r1;  // query rows of the item [r0, r1)
-  int h;       // q head
-  int kvh;     // key/value head
+  int flags;       // kFirst | kLast | kHasQ1, or kStop
+  int cls0, cls1;  // block class for Q tile 0 / Q tile 1
+  int c0, c1;      // key columns [c0, c1)
+  int r0, r_end;   // query rows of the item [r0, r_end); tile 1 starts at r0 + block_m
+  int h, kvh;      // q head, key/value head
+  int pad[7];
 };
-
-constexpr int kMetaSlots = 4;
+static_assert(sizeof(TileMeta) == 64, "TileMeta is 64 bytes");
 
 enum Bar : int {
   kKFull = 0,                     // [kStages]  K tile landed (TMA tx)
-  kKEmpty = kKFull + kStages,      // [kStages]  S MMA done reading K
+  kKEmpty = kKFull + kStages,      // [kStages]  S MMAs done reading K
   kVFull = kKEmpty + kStages,      // [kStages]  V tile landed
-  kVEmpty = kVFull + kStages,      // [kStages]  PV MMA done reading V
+  kVEmpty = kVFull + kStages,      // [kStages]  PV MMAs done reading V
   kMFull = kVEmpty + kStages,      // [kMetaSlots] tile metadata written
   kMEmpty = kMFull + kMetaSlots,   // [kMetaSlots] metadata consumed
-  kQFull = kMEmpty + kMetaSlots,
-  kQEmpty,
-  kSFull,  // [2]
-  kPFull = kSFull + 2,
-  kPEmpty,
-  kOEmpty,
-  kDrain,
+  kQFull = kMEmpty + kMetaSlots,   // both Q tiles of the item landed
+  kQEmpty,                         // last S MMA of the item done
+  kSFull,                          // [2] S_i ready
+  kPFull = kSFull + 2,             // [2] P_i written (128 arrivals)
+  kOFull = kPFull + 2,             // [2] last PV_i of the item done
+  kOEmpty = kOFull + 2,            // [2] O_i read by the epilogue (128 arrivals)
+  kDrain = kOEmpty + 2,
   kNumBars
 };
 
-// arrivals on kMEmpty: the V producer lane and the four softmax warps
-constexpr int kMEmptyCount = 5;
+// arrivals on kMEmpty: the V producer lane and the eight softmax warps
+constexpr int kMEmptyCount = 9;
 
 template <int D, int BN>
 struct Layout {
-  static constexpr int kQBytes = kTileM * D * 2;
+  static constexpr int kQBytes = kTileM * D * 2;  // one Q tile
   static constexpr int kKBytes = BN * D * 2;
   static constexpr int kVBytes = BN * D * 2;
-  static constexpr int kPBytes = kTileM * BN * 2;
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kQBytes;
+  static constexpr int kQ = 0;  // 2 Q tiles
+  static constexpr int kK = kQ + 2 * kQBytes;
   static constexpr int kV = kK + kStages * kKBytes;
-  static constexpr int kP = kV + kStages * kVBytes;
-  static constexpr int kCols = kP + kPBytes;  // int32 [kMetaSlots][4][BN]
+  static constexpr int kCols = kV + kStages * kVBytes;  // int32 [kMetaSlots][4][BN]
   static constexpr int kMeta = kCols + kMetaSlots * 4 * BN * 4;
   static constexpr int kBars = kMeta + kMetaSlots * static_cast<int>(sizeof(TileMeta));
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
@@ -105,9 +115,9 @@ struct Layout {
   static constexpr int kEnd = kAbort + 4;
   static constexpr int kBytes = kEnd + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kTmemS = 0;       // S buffers at columns [0, 2*BN)
-  static constexpr int kTmemO = 2 * BN;  // O at columns [2*BN, 2*BN + D)
-  static_assert(2 * BN + D <= 512, "TMEM budget");
+  // TMEM columns: S_i at i*128 (P_i packed into its first BN/2 columns),
+  // O_i at 256 + i*128.
+  static_assert(BN <= 128 && D <= 128, "TMEM budget");
   static_assert(kBytes <= 232448, "shared memory budget");
 };
 
@@ -132,36 +142,40 @@ __device__ __forceinline__ int classify_block(int r0, int r1, int c0, int c1, co
   return kClsU;
 }
 
-__device__ __forceinline__ void load_stats(const AttnParams& p, int mh, int64_t slot, int* st) {
-#pragma unroll
-  for (int v = 0; v < 8; ++v)
-    st[v] = __ldg(p.minmax + (static_cast<int64_t>(mh) * 8 + v) * p.n_kv_slots + slot);
-}
-
-// Class of KV tile kt of sample [a, b) for rows [r0, r1), or kClsF past kt_end.
+// Classes of KV tile kt of sample s ([a, b)) for the two Q tiles of an item:
+// rows [r0, r1) and [r1, r2) (the second is empty when r2 == r1).
 template <int BN>
-__device__ __forceinline__ int tile_class(const AttnParams& p, int mh, int s, int a, int b,
-                                          int r0, int r1, int kt, int kt_end) {
-  if (kt >= kt_end) return kClsF;
+__device__ __forceinline__ void tile_classes(const AttnParams& p, int mh, int s, int a, int b,
+                                             int r0, int r1, int r2, int kt, int kt_end,
+                                             int& cls0, int& cls1) {
+  cls0 = cls1 = kClsF;
+  if (kt >= kt_end) return;
   const int c0 = a + kt * BN;
   const int c1 = min(c0 + BN, b);
   int st[8];
   const bool has_mask = p.sri != nullptr;
-  if (has_mask) load_stats(p, mh, static_cast<int64_t>(a / BN) + s + kt, st);
-  return classify_block(r0, r1, c0, c1, st, has_mask, p.causal != 0);
+  if (has_mask) {
+    const int64_t slot = static_cast<int64_t>(a / BN) + s + kt;
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+      st[v] = __ldg(p.minmax + (static_cast<int64_t>(mh) * 8 + v) * p.n_kv_slots + slot);
+  }
+  const bool causal = p.causal != 0;
+  cls0 = classify_block(r0, r1, c0, c1, st, has_mask, causal);
+  if (r2 > r1) cls1 = classify_block(r1, r2, c0, c1, st, has_mask, causal);
 }
 
-// Number of KV tiles to examine for rows ending at r1 (causal: up to the
-// diagonal; every later tile is entirely above it and fully masked).
+// KV tiles to examine for rows ending at r_end (causal: up to the diagonal;
+// every later tile is entirely above it and fully masked).
 template <int BN>
-__device__ __forceinline__ int kv_tiles_to_scan(const AttnParams& p, int a, int b, int r1) {
+__device__ __forceinline__ int kv_tiles_to_scan(const AttnParams& p, int a, int b, int r_end) {
   const int n_kv = (b - a + BN - 1) / BN;
-  if (p.causal) return min(n_kv, (r1 - 1 - a) / BN + 1);
+  if (p.causal) return min(n_kv, (r_end - 1 - a) / BN + 1);
   return n_kv;
 }
 
 // ---------------------------------------------------------------------------
-// planner
+// planner: work unit = (sample, pair of consecutive Q tiles)
 // ---------------------------------------------------------------------------
 
 template <int BN>
@@ -170,33 +184,37 @@ __global__ void __launch_bounds__(256) plan_cost_kernel(const AttnParams p) {
   const int lane = threadIdx.x & 31;
   if (u >= p.n_qslots) return;
   const int T = static_cast<int>(p.T);
-  const int BM = p.block_m;
+  const int BM2 = 2 * p.block_m;
   int lo = 0, hi = p.n_seqs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    const int64_t base = static_cast<int64_t>(clamp_tok(__ldg(p.cu + mid), T)) / BM + mid;
+    const int64_t base = static_cast<int64_t>(clamp_tok(__ldg(p.cu + mid), T)) / BM2 + mid;
     if (base <= u) lo = mid; else hi = mid - 1;
   }
   const int s = lo;
   const int a = clamp_tok(__ldg(p.cu + s), T);
   const int b = max(a, clamp_tok(__ldg(p.cu + s + 1), T));
-  const int64_t qt = u - (static_cast<int64_t>(a) / BM + s);
-  if (qt < 0 || a + qt * BM >= b) {
+  const int64_t pair = u - (static_cast<int64_t>(a) / BM2 + s);
+  if (pair < 0 || a + pair * BM2 >= b) {
     if (lane == 0) p.cost[u] = -1;
     return;
   }
-  const int r0 = a + static_cast<int>(qt) * BM;
-  const int r1 = min(r0 + BM, b);
-  const int kt_end = kv_tiles_to_scan<BN>(p, a, b, r1);
+  const int r0 = a + static_cast<int>(pair) * BM2;
+  const int r1 = min(r0 + p.block_m, b);
+  const int r2 = min(r0 + BM2, b);
+  const int kt_end = kv_tiles_to_scan<BN>(p, a, b, r2);
   int cost = 0;
   for (int base = 0; base < kt_end; base += 32) {
-    const int cls = tile_class<BN>(p, 0, s, a, b, r0, r1, base + lane, kt_end);
-    cost += __popc(__ballot_sync(0xffffffffu, cls != kClsF));
+    int c0, c1;
+    tile_classes<BN>(p, 0, s, a, b, r0, r1, r2, base + lane, kt_end, c0, c1);
+    cost += __popc(__ballot_sync(0xffffffffu, c0 != kClsF));
+    cost += __popc(__ballot_sync(0xffffffffu, c1 != kClsF));
   }
   if (lane == 0) {
     p.cost[u] = cost;
-    p.slot_info[u] = make_int2(s, static_cast<int>(qt));
+    p.slot_info[u] = make_int2(s, static_cast<int>(pair));
     atomicAdd(p.hist + min(cost, kCostBins - 1), 1);
+    atomicAdd(&p.ws->n_qtiles, r2 > r1 ? 2 : 1);
   }
 }
 
@@ -229,8 +247,8 @@ __global__ void __launch_bounds__(kCostBins) plan_order_kernel(const AttnParams 
   const int incl = x + (w > 0 ? warp_tot[w - 1] : 0);
   offs[bin] = incl - cnt;
   if (tid == kCostBins - 1) {
-    p.ws->n_qtiles = incl;
     p.ws->n_items = incl * p.hq;
+    p.ws->n_tile_items = p.ws->n_qtiles * p.hq;
   }
   __syncthreads();
   for (int64_t u = tid; u < p.n_qslots; u += kCostBins) {
@@ -248,6 +266,50 @@ __global__ void __launch_bounds__(kCostBins) plan_order_kernel(const AttnParams 
   }
   if (tid == 0 && (__ldg(p.cu) != 0 || __ldg(p.cu + p.n_seqs) != p.T)) bad = true;
   if (bad) atomicOr(&p.ws->error_word, static_cast<int>(FM_DEVERR_DATA));
+}
+
+// ---------------------------------------------------------------------------
+// TMEM helpers local to this kernel
+// ---------------------------------------------------------------------------
+
+// D[tmem] (+)= A[tmem] * B[smem]^T (A = P, bf16 packed two per column, the
+// even element in the low half).
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
+// 64 consecutive 32-bit columns per lane, one wait for all of them.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Pull a tile into L2 ahead of its TMA load (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -272,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int T = static_cast<int>(p.T);
+  const int BM = p.block_m;
   const uint64_t tmo = p.timeout_ns;
 
   if (threadIdx.x == 0) {
@@ -287,11 +350,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars[kQFull], 1);
     mbar_init(&bars[kQEmpty], 1);
-    mbar_init(&bars[kSFull + 0], 1);
-    mbar_init(&bars[kSFull + 1], 1);
-    mbar_init(&bars[kPFull], 128);
-    mbar_init(&bars[kPEmpty], 1);
-    mbar_init(&bars[kOEmpty], 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[kSFull + i], 1);
+      mbar_init(&bars[kPFull + i], 128);
+      mbar_init(&bars[kOFull + i], 1);
+      mbar_init(&bars[kOEmpty + i], 128);
+    }
     mbar_init(&bars[kDrain], 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -328,6 +392,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     return false;
   };
 
+  // Each role below ends with teardown().
+  auto teardown = [&]() {
+    tc_fence_before();
+    asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+    if (warp == 1) {
+      __syncwarp();
+      tc_fence_after();
+      tmem_dealloc(*reinterpret_cast<volatile uint32_t*>(tmem_slot), L::kTmemCols);
+    }
+  };
+
   if (warp == 0) {
     // --------------------------------------------------- K producer + metadata
     const int n_items = p.ws->n_items;
@@ -340,8 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long cnt_p = 0, cnt_u = 0, cnt_f = 0;
     bool ok = true;
 
-    auto push_meta = [&](int cls, int flags, int c0, int c1, int r0, int r1, int h, int kvh,
-                         bool copy_cols, int mh) -> bool {
+    auto push_meta = [&](int flags, int cls0, int cls1, int c0, int c1, int r0, int r_end, int h,
+                         int kvh, bool copy_cols, int mh) -> bool {
       if (!warp_wait(kMEmpty + mslot, (mround & 1) ^ 1)) return false;
       if (copy_cols) {
         const int32_t* src = p.sri + static_cast<int64_t>(mh) * 4 * p.T;
@@ -358,12 +433,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (lane == 0) {
         TileMeta& m = meta[mslot];
-        m.cls = cls;
         m.flags = flags;
+        m.cls0 = cls0;
+        m.cls1 = cls1;
         m.c0 = c0;
         m.c1 = c1;
         m.r0 = r0;
-        m.r1 = r1;
+        m.r_end = r_end;
         m.h = h;
         m.kvh = kvh;
       }
@@ -382,35 +458,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) item = static_cast<int>(atomicAdd(&p.ws->work_counter, 1u));
       item = __shfl_sync(0xffffffffu, item, 0);
       if (item >= n_items) {
-        ok = push_meta(kClsStop, 0, 0, 0, 0, 0, 0, 0, false, 0);
+        ok = push_meta(kStop, kClsF, kClsF, 0, 0, 0, 0, 0, 0, false, 0);
         break;
       }
-      const int2 qi = p.order[item / p.hq];
+      const int2 pi = p.order[item / p.hq];
       const int h = item % p.hq;
-      const int s = qi.x;
+      const int s = pi.x;
       const int kvh = h / group;
       const int mh = p.hm > 1 ? h : 0;
       const int a = clamp_tok(__ldg(p.cu + s), T);
       const int b = max(a, clamp_tok(__ldg(p.cu + s + 1), T));
-      const int r0 = min(a + qi.y * p.block_m, b);
-      const int r1 = min(r0 + p.block_m, b);
+      const int r0 = min(a + pi.y * 2 * BM, b);
+      const int r1 = min(r0 + BM, b);
+      const int r2 = min(r0 + 2 * BM, b);
+      const bool has_q1 = r2 > r1;
       const int n_kv = (b - a + BN - 1) / BN;
-      const int kt_end = (r1 > r0) ? kv_tiles_to_scan<BN>(p, a, b, r1) : 0;
+      const int kt_end = (r2 > r0) ? kv_tiles_to_scan<BN>(p, a, b, r2) : 0;
 
-      // pass 1: block classes of the item (counts, number of live tiles)
-      int n_live = 0, n_p = 0;
+      // pass 1: block classes of both Q tiles (counts, number of live tiles)
+      int n_live = 0;
       for (int base = 0; base < kt_end; base += 32) {
-        const int cls = tile_class<BN>(p, mh, s, a, b, r0, r1, base + lane, kt_end);
-        n_live += __popc(__ballot_sync(0xffffffffu, cls != kClsF));
-        n_p += __popc(__ballot_sync(0xffffffffu, cls == kClsP));
+        int c0, c1;
+        tile_classes<BN>(p, mh, s, a, b, r0, r1, r2, base + lane, kt_end, c0, c1);
+        n_live += __popc(__ballot_sync(0xffffffffu, c0 != kClsF || c1 != kClsF));
+        const int p0 = __popc(__ballot_sync(0xffffffffu, c0 == kClsP));
+        const int u0 = __popc(__ballot_sync(0xffffffffu, c0 == kClsU));
+        const int p1 = __popc(__ballot_sync(0xffffffffu, c1 == kClsP));
+        const int u1 = __popc(__ballot_sync(0xffffffffu, c1 == kClsU));
+        cnt_p += p0 + p1;
+        cnt_u += u0 + u1;
+        cnt_f -= p0 + u0 + p1 + u1;
       }
-      cnt_p += n_p;
-      cnt_u += n_live - n_p;
-      cnt_f += n_kv - n_live;
+      if (r2 > r0) cnt_f += static_cast<long long>(n_kv) * (has_q1 ? 2 : 1);
 
       if (n_live == 0) {
         // every key of these rows is masked: o = 0, lse = -inf
-        for (int r = r0 + lane; r < r1; r += 32) {
+        for (int r = r0 + lane; r < r2; r += 32) {
           uint4* dst = reinterpret_cast<uint4*>(
               static_cast<__nv_bfloat16*>(p.out) +
               (static_cast<IdxT>(r) * p.hq + h) * static_cast<IdxT>(D));
@@ -421,35 +504,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
 
-      // pass 2: metadata and K for every tile that is not fully masked
+      // pass 2: metadata and K for every tile live for either Q tile
       int pushed = 0;
       for (int base = 0; base < kt_end && ok; base += 32) {
-        const int my_cls = tile_class<BN>(p, mh, s, a, b, r0, r1, base + lane, kt_end);
-        uint32_t live = __ballot_sync(0xffffffffu, my_cls != kClsF);
+        int my0, my1;
+        tile_classes<BN>(p, mh, s, a, b, r0, r1, r2, base + lane, kt_end, my0, my1);
+        uint32_t live = __ballot_sync(0xffffffffu, my0 != kClsF || my1 != kClsF);
+        if (lane == 0) {
+          // the first live tiles of the chunk (the very first is loaded next)
+          uint32_t m = live & (live - 1u);
+          for (int t = 1; t < kPrefetchAhead && m != 0u; ++t, m &= m - 1u) {
+            const int ca = a + (base + __ffs(m) - 1) * BN;
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+              tma_prefetch_l2(&tk, kvh * D + c * 64, ca);
+              tma_prefetch_l2(&tv, kvh * D + c * 64, ca);
+            }
+          }
+        }
         while (live != 0u) {
           const int l = __ffs(live) - 1;
           live &= live - 1u;
-          const int cls = __shfl_sync(0xffffffffu, my_cls, l);
+          const int cls0 = __shfl_sync(0xffffffffu, my0, l);
+          const int cls1 = __shfl_sync(0xffffffffu, my1, l);
           const int c0 = a + (base + l) * BN;
           const int c1 = min(c0 + BN, b);
-          const int flags = (pushed == 0 ? kFirst : 0) | (pushed == n_live - 1 ? kLast : 0);
-          if (!push_meta(cls, flags, c0, c1, r0, r1, h, kvh, cls == kClsP && p.sri != nullptr,
-                         mh)) {
+          if (lane == 0) {
+            // warm L2 with the K/V tile kPrefetchAhead live tiles further on
+            // (within this 32-tile chunk); its TMA load then hits L2
+            uint32_t m = live;
+            for (int t = 1; t < kPrefetchAhead && m != 0u; ++t) m &= m - 1u;
+            if (m != 0u) {
+              const int ca = a + (base + __ffs(m) - 1) * BN;
+#pragma unroll
+              for (int c = 0; c < D / 64; ++c) {
+                tma_prefetch_l2(&tk, kvh * D + c * 64, ca);
+                tma_prefetch_l2(&tv, kvh * D + c * 64, ca);
+              }
+            }
+          }
+          const int flags = (pushed == 0 ? kFirst : 0) | (pushed == n_live - 1 ? kLast : 0) |
+                            (has_q1 ? kHasQ1 : 0);
+          const bool copy = (cls0 == kClsP || cls1 == kClsP) && p.sri != nullptr;
+          if (!push_meta(flags, cls0, cls1, c0, c1, r0, r2, h, kvh, copy, mh)) {
             ok = false;
             break;
           }
           if (pushed == 0) {
-            // Q tile of this item, once the previous item's S MMAs are done
+            // Q tiles of this item, once the previous item's S MMAs are done
             if (!warp_wait(kQEmpty, (q_round & 1) ^ 1)) {
               ok = false;
               break;
             }
             if (lane == 0) {
-              mbar_arrive_expect_tx(&bars[kQFull], L::kQBytes);
+              mbar_arrive_expect_tx(&bars[kQFull], (has_q1 ? 2 : 1) * L::kQBytes);
 #pragma unroll
               for (int c = 0; c < D / 64; ++c)
                 tma_load_2d(smem + L::kQ + c * (kTileM * 128), &tq, &bars[kQFull],
                             h * D + c * 64, r0);
+              if (has_q1) {
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                  tma_load_2d(smem + L::kQ + L::kQBytes + c * (kTileM * 128), &tq,
+                              &bars[kQFull], h * D + c * 64, r0 + BM);
+              }
             }
             q_armed = q_round;
             ++q_round;
@@ -490,6 +608,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       atomicAdd(reinterpret_cast<unsigned long long*>(p.class_counts + 2),
                 static_cast<unsigned long long>(cnt_u));
     }
+    teardown();
+    return;
   } else if (warp == 2) {
     // --------------------------------------------------------------- V producer
     if (lane == 0) {
@@ -498,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (;;) {
         if (!lone_wait(kMFull + mslot, mround & 1)) { ok = false; break; }
-        const int cls = *reinterpret_cast<volatile int*>(&meta[mslot].cls);
+        const int flags = *reinterpret_cast<volatile int*>(&meta[mslot].flags);
         const int c0 = *reinterpret_cast<volatile int*>(&meta[mslot].c0);
         const int kvh = *reinterpret_cast<volatile int*>(&meta[mslot].kvh);
         mbar_arrive(&bars[kMEmpty + mslot]);
@@ -506,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mslot = 0;
           ++mround;
         }
-        if (cls == kClsStop) break;
+        if (flags & kStop) break;
         if (!lone_wait(kVEmpty + vst, (vround & 1) ^ 1)) { ok = false; break; }
         mbar_arrive_expect_tx(&bars[kVFull + vst], L::kVBytes);
 #pragma unroll
@@ -525,6 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_bounded(&bars[kVFull + st], v_armed[st] & 1, 100000000ull, nullptr);
       }
     }
+    teardown();
+    return;
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -533,256 +655,325 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_addr = smem_u32(smem + L::kQ);
       const uint32_t k_addr = smem_u32(smem + L::kK);
       const uint32_t v_addr = smem_u32(smem + L::kV);
-      const uint32_t p_addr = smem_u32(smem + L::kP);
-      uint32_t mslot = 0, mround = 0;  // metadata ring
+      uint32_t mslot = 0, mround = 0;  // metadata ring (released by the other readers)
       uint32_t kst = 0, kround = 0, vst = 0, vround = 0;
-      uint32_t q_round = 0, p_round = 0, o_round = 0, sbuf = 0;
-      int items_done = 0;
+      uint32_t q_round = 0;
+      uint32_t p_round[2] = {0u, 0u}, o_round[2] = {0u, 0u};
+      bool o_pending[2] = {false, false};  // an epilogue of tile i has not been waited for
       bool ok = true;
 
-      // flags of the next tile (kClsStop -> stop); the softmax warps release
-      // the metadata slot
-      auto next_meta = [&](int& flags) -> int {
-        if (!lone_wait(kMFull + mslot, mround & 1)) return -1;
-        const int cls = *reinterpret_cast<volatile int*>(&meta[mslot].cls);
+      auto next_flags = [&](int& flags) -> bool {
+        if (!lone_wait(kMFull + mslot, mround & 1)) return false;
         flags = *reinterpret_cast<volatile int*>(&meta[mslot].flags);
         if (++mslot == kMetaSlots) {
           mslot = 0;
           ++mround;
         }
-        return cls;
+        return true;
       };
-      auto issue_s = [&](uint32_t buf) -> bool {
-        if (!lone_wait(kKFull + kst, kround & 1)) return false;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + L::kTmemS + buf * BN;
+      // S_i = Q_i K^T for the K tile in stage kst
+      auto issue_s = [&](int i) {
+        const uint32_t d_tmem = tmem_base + i * 128;
+        const uint32_t qa = q_addr + i * L::kQBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk & 3) * 32;
           const uint32_t chunk = kk >> 2;
-          const uint64_t ad = sdesc_sw128(q_addr + chunk * (kTileM * 128) + koff, 16, 1024);
+          const uint64_t ad = sdesc_sw128(qa + chunk * (kTileM * 128) + koff, 16, 1024);
           const uint64_t bd =
               sdesc_sw128(k_addr + kst * L::kKBytes + chunk * (BN * 128) + koff, 16, 1024);
           umma_bf16(d_tmem, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bars[kSFull + buf]);
+        umma_commit(&bars[kSFull + i]);
+      };
+      // O_i (+)= P_i V for the V tile in stage vst
+      auto issue_pv = [&](int i, bool first) {
+        const uint32_t d_tmem = tmem_base + 256 + i * 128;
+        const uint32_t a_tmem = tmem_base + i * 128;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t bd =
+              sdesc_sw128(v_addr + vst * L::kVBytes + kk * (16 * 128), BN * 128, 1024);
+          umma_bf16_tmem_a(d_tmem, a_tmem + kk * 8, bd, kIdescO, (!first || kk > 0) ? 1u : 0u);
+        }
+      };
+      // S MMAs of the first tile of an item (waits for its Q tiles and K)
+      auto start_item = [&](int flags) -> bool {
+        if (!lone_wait(kQFull, q_round & 1)) return false;
+        ++q_round;
+        if (!lone_wait(kKFull + kst, kround & 1)) return false;
+        tc_fence_after();
+        issue_s(0);
+        if (flags & kHasQ1) issue_s(1);
         umma_commit(&bars[kKEmpty + kst]);
+        if (flags & kLast) umma_commit(&bars[kQEmpty]);
         if (++kst == kStages) {
           kst = 0;
           ++kround;
         }
         return true;
       };
-      auto issue_pv = [&](bool first) -> bool {
-        if (!lone_wait(kVFull + vst, vround & 1)) return false;
+      auto wait_pv_ready = [&](int i, bool first) -> bool {
+        if (first && o_pending[i]) {
+          if (!lone_wait(kOEmpty + i, o_round[i] & 1)) return false;
+          ++o_round[i];
+          o_pending[i] = false;
+        }
+        if (!lone_wait(kPFull + i, p_round[i] & 1)) return false;
+        ++p_round[i];
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + L::kTmemO;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint32_t koff = (kk & 3) * 32;
-          const uint32_t chunk = kk >> 2;
-          const uint64_t ad = sdesc_sw128(p_addr + chunk * (kTileM * 128) + koff, 16, 1024);
-          const uint64_t bd =
-              sdesc_sw128(v_addr + vst * L::kVBytes + kk * (16 * 128), BN * 128, 1024);
-          umma_bf16(d_tmem, ad, bd, kIdescO, (!first || kk > 0) ? 1u : 0u);
+        return true;
+      };
+
+      int cur = 0;
+      ok = next_flags(cur);
+      if (ok && !(cur & kStop)) ok = start_item(cur);
+      while (ok && !(cur & kStop)) {
+        const bool first = (cur & kFirst) != 0;
+        const bool last = (cur & kLast) != 0;
+        const bool q1 = (cur & kHasQ1) != 0;
+        int nxt = 0;
+        if (!last && !next_flags(nxt)) { ok = false; break; }
+        if (!lone_wait(kVFull + vst, vround & 1)) { ok = false; break; }
+        // tile 0: PV, then S of the next KV tile (P_0 is read before S_0 is
+        // overwritten: MMAs from one thread run in issue order)
+        if (!wait_pv_ready(0, first)) { ok = false; break; }
+        issue_pv(0, first);
+        if (last) {
+          umma_commit(&bars[kOFull + 0]);
+          o_pending[0] = true;
+        }
+        if (!last) {
+          if (!lone_wait(kKFull + kst, kround & 1)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(0);
+        }
+        // tile 1
+        if (q1) {
+          if (!wait_pv_ready(1, first)) { ok = false; break; }
+          issue_pv(1, first);
+          if (last) {
+            umma_commit(&bars[kOFull + 1]);
+            o_pending[1] = true;
+          }
+          if (!last) issue_s(1);
         }
         umma_commit(&bars[kVEmpty + vst]);
-        umma_commit(&bars[kPEmpty]);
         if (++vst == kStages) {
           vst = 0;
           ++vround;
         }
-        return true;
-      };
-      // S MMA of the first tile of a new item (waits for its Q tile)
-      auto start_item = [&](int flags, uint32_t buf) -> bool {
-        if (!lone_wait(kQFull, q_round & 1)) return false;
-        ++q_round;
-        tc_fence_after();
-        if (!issue_s(buf)) return false;
-        if (flags & kLast) umma_commit(&bars[kQEmpty]);
-        return true;
-      };
-
-      int cur_flags = 0;
-      int cls = next_meta(cur_flags);
-      ok = (cls >= 0);
-      bool stop = (cls == kClsStop);
-      if (ok && !stop) ok = start_item(cur_flags, sbuf);
-      while (ok && !stop) {
-        int nxt_flags = 0;
-        if (!(cur_flags & kLast)) {
-          // S of the next tile of the same item overlaps this tile's softmax
-          cls = next_meta(nxt_flags);
-          if (cls < 0 || cls == kClsStop) { ok = false; break; }
-          if (!issue_s(sbuf ^ 1u)) { ok = false; break; }
-          if (nxt_flags & kLast) umma_commit(&bars[kQEmpty]);
+        if (!last) {
+          umma_commit(&bars[kKEmpty + kst]);
+          if (nxt & kLast) umma_commit(&bars[kQEmpty]);
+          if (++kst == kStages) {
+            kst = 0;
+            ++kround;
+          }
+        } else {
+          if (!next_flags(nxt)) { ok = false; break; }
+          if (nxt & kStop) break;
+          if (!start_item(nxt)) { ok = false; break; }
         }
-        if (!lone_wait(kPFull, p_round & 1)) { ok = false; break; }
-        ++p_round;
-        tc_fence_after();
-        if ((cur_flags & kFirst) && items_done > 0) {
-          if (!lone_wait(kOEmpty, o_round & 1)) { ok = false; break; }
-          ++o_round;
-          tc_fence_after();
-        }
-        if (!issue_pv((cur_flags & kFirst) != 0)) { ok = false; break; }
-        if (cur_flags & kLast) {
-          ++items_done;
-          cls = next_meta(nxt_flags);
-          if (cls < 0) { ok = false; break; }
-          if (cls == kClsStop) break;
-          if (!start_item(nxt_flags, sbuf ^ 1u)) { ok = false; break; }
-        }
-        cur_flags = nxt_flags;
-        sbuf ^= 1u;
+        cur = nxt;
       }
       // all issued MMAs complete before TMEM is released
       umma_commit(&bars[kDrain]);
       mbar_wait_bounded(&bars[kDrain], 0, 100000000ull, nullptr);
     }
-  } else if (warp >= 4) {
+    teardown();
+    return;
+  } else {
     // ------------------------------------------------------------------ softmax
+    const int wg = (warp - kFirstSoftmaxWarp) >> 2;  // which Q tile of the item
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t s_tmem = tmem_base + lane_addr + L::kTmemS;
-    const uint32_t o_tmem = tmem_base + lane_addr + L::kTmemO;
-    const uint32_t p_row = smem_u32(smem + L::kP) + row * 128;
+    const uint32_t s_tmem = tmem_base + lane_addr + wg * 128;
+    const uint32_t o_tmem = tmem_base + lane_addr + 256 + wg * 128;
     const float scale_log2 = p.scale_log2;
     const bool has_mask = p.sri != nullptr;
     const bool causal = p.causal != 0;
-    uint32_t mslot = 0, mround = 0, sbuf = 0;
-    uint32_t s_round[2] = {0u, 0u};
-    uint32_t n_tiles = 0;
+    uint32_t mslot = 0, mround = 0;
+    uint32_t s_round = 0, o_round = 0;
     float m_run = -CUDART_INF_F, l_run = 0.f;
-    int r0 = 0, r1 = 0, h = 0;
+    int rt0 = 0, rt1 = 0, h = 0;
 
     for (;;) {
       if (!warp_wait(kMFull + mslot, mround & 1)) break;
-      TileMeta md;
-      md.cls = *reinterpret_cast<volatile int*>(&meta[mslot].cls);
-      if (md.cls == kClsStop) break;
-      md.flags = *reinterpret_cast<volatile int*>(&meta[mslot].flags);
-      md.c0 = *reinterpret_cast<volatile int*>(&meta[mslot].c0);
-      md.c1 = *reinterpret_cast<volatile int*>(&meta[mslot].c1);
-      md.r0 = *reinterpret_cast<volatile int*>(&meta[mslot].r0);
-      md.r1 = *reinterpret_cast<volatile int*>(&meta[mslot].r1);
-      md.h = *reinterpret_cast<volatile int*>(&meta[mslot].h);
+      const TileMeta* mp = meta + mslot;
+      const int flags = *reinterpret_cast<const volatile int*>(&mp->flags);
+      if (flags & kStop) break;
+      const int cls = wg == 0 ? *reinterpret_cast<const volatile int*>(&mp->cls0)
+                              : *reinterpret_cast<const volatile int*>(&mp->cls1);
+      const int c0 = *reinterpret_cast<const volatile int*>(&mp->c0);
+      const int c1 = *reinterpret_cast<const volatile int*>(&mp->c1);
+      const bool first = (flags & kFirst) != 0;
+      if (first) {
+        const int r0 = *reinterpret_cast<const volatile int*>(&mp->r0);
+        const int r_end = *reinterpret_cast<const volatile int*>(&mp->r_end);
+        h = *reinterpret_cast<const volatile int*>(&mp->h);
+        rt0 = r0 + wg * BM;
+        rt1 = min(rt0 + BM, r_end);
+      }
       const uint32_t cur_slot = mslot;
       if (++mslot == kMetaSlots) {
         mslot = 0;
         ++mround;
       }
-
-      const bool first = (md.flags & kFirst) != 0;
+      if (wg == 1 && !(flags & kHasQ1)) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kMEmpty + cur_slot]);
+        continue;
+      }
       if (first) {
         m_run = -CUDART_INF_F;
         l_run = 0.f;
-        r0 = md.r0;
-        r1 = md.r1;
-        h = md.h;
       }
-      if (!warp_wait(kSFull + sbuf, s_round[sbuf] & 1)) break;
-      ++s_round[sbuf];
+      if (!warp_wait(kSFull + wg, s_round & 1)) break;
+      ++s_round;
       tc_fence_after();
 
-      float sv[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(s_tmem + sbuf * BN + c * 32, rr);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(rr[i]) * scale_log2;
-      }
-
-      const int r = r0 + row;
-      if (md.cls == kClsP) {
+      const int r = rt0 + row;
+      const int valid = c1 - c0;  // columns inside the sample
+      uint32_t mbits[BN / 32];    // element mask of a partially masked block
+      if (cls == kClsP) {
+        // element mask of the row as bits, before any score is loaded
         const int* cl = cols + cur_slot * 4 * BN;
 #pragma unroll
-        for (int jj = 0; jj < BN; ++jj) {
-          const int c = md.c0 + jj;
-          bool masked;
-          if (c >= md.c1) {
-            masked = true;
-          } else if (r >= c) {
-            masked = has_mask && (cl[jj] <= r) && (r < cl[BN + jj]);
-          } else {
-            masked = causal || (has_mask && (cl[2 * BN + jj] <= r) && (r < cl[3 * BN + jj]));
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t bits = 0;
+#pragma unroll 4
+          for (int i = 0; i < 32; ++i) {
+            const int jj = c * 32 + i;
+            const int col = c0 + jj;
+            bool masked;
+            if (jj >= valid) {
+              masked = true;
+            } else if (r >= col) {
+              masked = has_mask && (cl[jj] <= r) && (r < cl[BN + jj]);
+            } else {
+              masked = causal || (has_mask && (cl[2 * BN + jj] <= r) && (r < cl[3 * BN + jj]));
+            }
+            bits |= (masked ? 1u : 0u) << i;
           }
-          if (masked) sv[jj] = -CUDART_INF_F;
+          mbits[c] = bits;
         }
-      } else if (md.c1 - md.c0 < BN) {
-        const int valid = md.c1 - md.c0;
-#pragma unroll
-        for (int jj = 0; jj < BN; ++jj)
-          if (jj >= valid) sv[jj] = -CUDART_INF_F;
       }
       // metadata and mask columns of this tile are no longer needed
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kMEmpty + cur_slot]);
 
-      float mt = sv[0];
+      if (cls == kClsF) {
+        // live only for the other Q tile: contributes nothing, P = 0
+        uint32_t z[16];
 #pragma unroll
-      for (int jj = 1; jj < BN; ++jj) mt = fmaxf(mt, sv[jj]);
-      const float m_new = fmaxf(m_run, mt);
-      // keep the old reference max unless it grew by more than 2^8
-      const bool resc = first || (m_new > m_run + 8.0f);
-      float factor = 1.f;
-      float m_ref = m_run;
-      if (resc) {
-        factor = (m_run == -CUDART_INF_F) ? 0.f : ex2_approx(m_run - m_new);
-        m_ref = m_new;
-      }
-      const bool need_o = resc && !first && (m_run != -CUDART_INF_F);
-      if (__any_sync(0xffffffffu, need_o)) {
-        // O may be rescaled only once the previous PV MMA has finished
-        if (!warp_wait(kPEmpty, (n_tiles - 1) & 1)) break;
-        tc_fence_after();
-        const float f = need_o ? factor : 1.f;
+        for (int i = 0; i < 16; ++i) z[i] = 0u;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(o_tmem + c * 32, rr);
+        for (int c = 0; c < BN / 32; ++c) tmem_st16(s_tmem + c * 16, z);
+        tmem_st_wait();
+      } else {
+        // pass 1: row max, 64 columns per TMEM load
+        float m8[8];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * f);
-          tmem_st32(o_tmem + c * 32, rr);
+        for (int i = 0; i < 8; ++i) m8[i] = -CUDART_INF_F;
+#pragma unroll
+        for (int h64 = 0; h64 < BN / 64; ++h64) {
+          uint32_t sr[64];
+          tmem_ld64(s_tmem + h64 * 64, sr);
+          if (cls == kClsP) {
+            const uint32_t b0 = mbits[2 * h64], b1 = mbits[2 * h64 + 1];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+              const bool masked = ((j < 32 ? b0 >> j : b1 >> (j - 32)) & 1u) != 0u;
+              m8[j & 7] = fmaxf(m8[j & 7], masked ? -CUDART_INF_F : __uint_as_float(sr[j]));
+            }
+          } else if (valid < BN) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+              m8[j & 7] = fmaxf(m8[j & 7],
+                                h64 * 64 + j >= valid ? -CUDART_INF_F : __uint_as_float(sr[j]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j]));
+          }
+        }
+        const float mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        // scores in the log2 domain: x = s * scale * log2(e)
+        const float mt2 = mt * scale_log2;
+        const float m_new = fmaxf(m_run, mt2);
+        // keep the old reference max unless it grew by more than 2^8
+        const bool resc = first || (m_new > m_run + 8.0f);
+        float factor = 1.f;
+        float m_ref = m_run;
+        if (resc) {
+          factor = (m_run == -CUDART_INF_F) ? 0.f : ex2_approx(m_run - m_new);
+          m_ref = m_new;
+        }
+        const bool need_o = resc && !first && (m_run != -CUDART_INF_F);
+        if (resc) l_run = first ? 0.f : l_run * factor;
+        m_run = m_ref;
+
+        const float neg_base = (m_ref == -CUDART_INF_F) ? 0.f : -m_ref;
+        float sum8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sum8[i] = 0.f;
+        // pass 2: P = 2^(x - m), 64 columns per TMEM load; P overwrites the
+        // first half of the S columns (already consumed)
+#pragma unroll
+        for (int h64 = 0; h64 < BN / 64; ++h64) {
+          uint32_t sr[64];
+          tmem_ld64(s_tmem + h64 * 64, sr);
+          if (cls == kClsP) {
+            const uint32_t b0 = mbits[2 * h64], b1 = mbits[2 * h64 + 1];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+              const bool masked = ((j < 32 ? b0 >> j : b1 >> (j - 32)) & 1u) != 0u;
+              if (masked) sr[j] = __float_as_uint(-CUDART_INF_F);
+            }
+          } else if (valid < BN) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+              if (h64 * 64 + j >= valid) sr[j] = __float_as_uint(-CUDART_INF_F);
+          }
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const int j = c * 32 + i;
+              const float p0 = ex2_approx(fmaf(__uint_as_float(sr[j]), scale_log2, neg_base));
+              const float p1 = ex2_approx(fmaf(__uint_as_float(sr[j + 1]), scale_log2, neg_base));
+              sum8[(i >> 1) & 7] += p0 + p1;
+              pk[i >> 1] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(s_tmem + h64 * 32 + c * 16, pk);
+          }
         }
         tmem_st_wait();
-      }
-      if (resc) l_run = first ? 0.f : l_run * factor;
-      m_run = m_ref;
-
-      const float base = (m_ref == -CUDART_INF_F) ? 0.f : m_ref;
-      float sum = 0.f;
-      uint32_t pk[BN / 2];
+        l_run += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                 ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        if (__any_sync(0xffffffffu, need_o)) {
+          // rescale O before the PV of this tile is issued (it waits for P);
+          // the previous PV completed before S, which was committed after it
+          const float f = need_o ? factor : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t rr[32];
+            tmem_ld32(o_tmem + c * 32, rr);
 #pragma unroll
-      for (int jj = 0; jj < BN; jj += 2) {
-        const float p0 = ex2_approx(sv[jj] - base);
-        const float p1 = ex2_approx(sv[jj + 1] - base);
-        sum += p0 + p1;
-        pk[jj / 2] = pack_bf16x2(p0, p1);
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * f);
+            tmem_st32(o_tmem + c * 32, rr);
+          }
+          tmem_st_wait();
+        }
       }
-      l_run += sum;
-
-      // the P buffer is free once the previous PV MMA has finished
-      if (n_tiles > 0) {
-        if (!warp_wait(kPEmpty, (n_tiles - 1) & 1)) break;
-      }
-#pragma unroll
-      for (int u = 0; u < BN / 8; ++u) {
-        const uint32_t kc = u >> 3;
-        const uint32_t swz = static_cast<uint32_t>((u & 7) ^ (row & 7));
-        st_shared_v4(p_row + kc * (kTileM * 128) + swz * 16, pk[4 * u + 0], pk[4 * u + 1],
-                     pk[4 * u + 2], pk[4 * u + 3]);
-      }
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars[kPFull]);
-      ++n_tiles;
-      sbuf ^= 1u;
+      mbar_arrive(&bars[kPFull + wg]);
 
-      if (md.flags & kLast) {
-        if (!warp_wait(kPEmpty, (n_tiles - 1) & 1)) break;
+      if (flags & kLast) {
+        if (!warp_wait(kOFull + wg, o_round & 1)) break;
+        ++o_round;
         tc_fence_after();
         const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
         __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
@@ -791,7 +982,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < D / 32; ++c) {
           uint32_t rr[32];
           tmem_ld32(o_tmem + c * 32, rr);
-          if (r < r1) {
+          if (r < rt1) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -807,22 +998,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (r < r1) {
+        if (r < rt1) {
           p.lse[static_cast<IdxT>(h) * static_cast<IdxT>(p.T) + r] =
               (l_run > 0.f) ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -CUDART_INF_F;
         }
         tc_fence_before();
-        mbar_arrive(&bars[kOEmpty]);
+        mbar_arrive(&bars[kOEmpty + wg]);
       }
     }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem_base, L::kTmemCols);
+    teardown();
+    return;
   }
 }
 
@@ -843,21 +1028,24 @@ template <int D, int BN, typename IdxT>
 cudaError_t launch_typed(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, int num_sms, cudaStream_t stream) {
   using L = Layout<D, BN>;
-  static bool configured = false;  // benign race: the attribute call is idempotent
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, BN, IdxT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static unsigned long long configured = 0ull;  // one bit per device; setting twice is harmless
+  if (dev >= 64 || !((configured >> dev) & 1ull)) {
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D, BN, IdxT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
-    configured = true;
+    if (dev < 64) configured |= 1ull << dev;
   }
-  const int64_t qwarps = p.n_qslots;
-  plan_cost_kernel<BN><<<static_cast<unsigned>((qwarps + 7) / 8), 256, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  const int64_t n_slots = p.n_qslots;
+  plan_cost_kernel<BN><<<static_cast<unsigned>((n_slots + 7) / 8), 256, 0, stream>>>(p);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   plan_order_kernel<<<1, kCostBins, 0, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t max_items = p.n_qslots * p.hq;
+  const int64_t max_items = n_slots * p.hq;
   const int grid = static_cast<int>(max_items < num_sms ? max_items : num_sms);
   attn_fwd_kernel<D, BN, IdxT><<<grid, kThreads, L::kBytes, stream>>>(p, tq, tk, tv);
   return cudaGetLastError();

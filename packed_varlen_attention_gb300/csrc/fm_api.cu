@@ -263,7 +263,7 @@ fm_status fm_attn_fwd_num_work_items(const void* workspace, int64_t* host_items,
   const auto* hdr = static_cast<const fm::AttnWorkspaceHeader*>(workspace);
   int32_t n = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(&n, &hdr->n_items, sizeof(n), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+  if (cudaMemcpyAsync(&n, &hdr->n_tile_items, sizeof(n), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess)
     return FM_ERR_CUDA;
   *host_items = n;

@@ -31,9 +31,10 @@ cudaError_t launch_mask_minmax(const int32_t* sri, int n_mask_heads, int64_t T,
 struct AttnWorkspaceHeader {
   uint32_t work_counter;  // next work item (atomic)
   int32_t n_qtiles;       // real Q tiles found by the planner
-  int32_t n_items;        // n_qtiles * Hq
+  int32_t n_items;        // work items: (pair of Q tiles) x Hq
   int32_t error_word;     // FM_DEVERR_* bits
-  int32_t pad[60];
+  int32_t n_tile_items;   // n_qtiles * Hq
+  int32_t pad[59];
 };
 static_assert(sizeof(AttnWorkspaceHeader) == 256, "header is 256 bytes");
 
