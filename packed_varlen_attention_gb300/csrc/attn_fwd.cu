@@ -18,7 +18,7 @@
 //     nothing.
 //   * Persistent main kernel, one CTA per SM, pulling items (two consecutive
 //     Q tiles of one sample x one q head) from an atomic counter.  The two Q
-//     tiles share every K/V tile the CTA loads.  Warp roles (352 threads):
+//     tiles share every K/V tile the CTA loads.  Warp roles (384 threads):
 //       warp 0      K producer: classifies the item's KV tiles for both Q
 //                   tiles (warp-parallel, 32 tiles per step), publishes
 //                   per-tile metadata (and the mask columns of partially
@@ -29,7 +29,7 @@
 //                   fp32 accumulate: S_i = Q_i K^T into TMEM (i = 0, 1), then
 //                   O_i += P_i V with P_i read from TMEM (it overwrites the
 //                   first half of S_i's columns as packed bf16);
-//       warps 3..6  softmax of Q tile 0, warps 7..10 softmax of Q tile 1: one
+//       warps 4..7  softmax of Q tile 0, warps 8..11 softmax of Q tile 1: one
 //                   thread per tile row (= TMEM lane).  The whole S row is
 //                   loaded from TMEM with one wait, masked (partial blocks
 //                   only), reduced to its max, turned into
@@ -55,12 +55,10 @@
 namespace fm {
 namespace {
 
-// warps 0..2: K producer, MMA issuer, V producer; warps 3..10: softmax (two
-// warpgroups; warp w reads TMEM lanes 32*(w%4)..+31, so each group of four
-// consecutive warps covers all 128 rows).  352 threads leave 184 registers
-// per thread, enough for a whole 128-column S row.
-constexpr int kThreads = 352;
-constexpr int kFirstSoftmaxWarp = 3;
+// warps 0..3: K producer, MMA issuer, V producer, idle; warps 4..11: softmax
+// (two warpgroups; warp w reads TMEM lanes 32*(w%4)..+31).
+constexpr int kThreads = 384;
+constexpr int kFirstSoftmaxWarp = 4;
 constexpr int kStages = 2;
 constexpr int kTileM = 128;  // MMA M: TMEM lanes = tile rows
 constexpr int kMetaSlots = 4;
@@ -304,6 +302,45 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
       : "memory");
 }
 
+// 128 consecutive 32-bit columns per lane, one wait for all of them.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%128];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr)
+      : "memory");
+}
+
+// The whole S row of one thread (BN columns) with one wait.
+template <int BN>
+__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, uint32_t (&r)[BN]);
+template <>
+__device__ __forceinline__ void tmem_ld_row<64>(uint32_t taddr, uint32_t (&r)[64]) {
+  tmem_ld64(taddr, r);
+}
+template <>
+__device__ __forceinline__ void tmem_ld_row<128>(uint32_t taddr, uint32_t (&r)[128]) {
+  tmem_ld128(taddr, r);
+}
+
+// Register split between the warpgroups (all four warps of a warpgroup run
+// the same instruction).  The kernel is launched with kThreads x kLaunchRegs
+// registers; kProducerRegs x 128 + kSoftmaxRegs x 256 must not exceed that,
+// which the host checks against the compiled register count before launch.
+constexpr int kLaunchRegs = 168;
+constexpr int kProducerRegs = 96;
+constexpr int kSoftmaxRegs = 200;
+static_assert(kProducerRegs * 128 + kSoftmaxRegs * 256 <= kThreads * kLaunchRegs,
+              "register split exceeds the launch budget");
+
+__device__ __forceinline__ void regs_release() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
+}
+__device__ __forceinline__ void regs_acquire() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
+}
+
 // Pull a tile into L2 ahead of its TMA load (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
@@ -316,11 +353,51 @@ __device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, i
 // persistent attention kernel
 // ---------------------------------------------------------------------------
 
+// End of every role: all threads meet, then the warp that allocated TMEM frees it.
+template <int D, int BN>
+__device__ __forceinline__ void attn_teardown(uint32_t* tmem_slot, int warp) {
+  tc_fence_before();
+  asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(*reinterpret_cast<volatile uint32_t*>(tmem_slot), Layout<D, BN>::kTmemCols);
+  }
+}
+
+// Bounded waits shared by every role; on expiry the CTA is told to stop and
+// FM_DEVERR_TIMEOUT is recorded.
+struct Sync {
+  uint64_t* bars;
+  volatile int* abort;
+  uint64_t tmo;
+  int* err;
+  int lane;
+  __device__ __forceinline__ void fail() const {
+    *abort = 1;
+    atomicOr(err, static_cast<int>(FM_DEVERR_TIMEOUT));
+  }
+  // single-thread wait
+  __device__ __forceinline__ bool lone(int bar, uint32_t parity) const {
+    if (mbar_wait_bounded(&bars[bar], parity, tmo, abort)) return true;
+    fail();
+    return false;
+  }
+  // every lane waits; the warp proceeds only if all lanes saw the phase
+  __device__ __forceinline__ bool warp(int bar, uint32_t parity) const {
+    const bool ok = mbar_wait_bounded(&bars[bar], parity, tmo, abort);
+    const bool all = __all_sync(0xffffffffu, ok);
+    if (!all && lane == 0) fail();
+    return all;
+  }
+};
+
+// Warps 0..3 (reduced register budget): K producer, MMA issuer, V producer
+// and one idle warp; warp 0 initialises the barriers, warp 1 owns TMEM.
 template <int D, int BN, typename IdxT>
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tq,
-                    const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv) {
+__device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const CUtensorMap& tq,
+                                                    const CUtensorMap& tk,
+                                                    const CUtensorMap& tv) {
   using L = Layout<D, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -330,13 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
   TileMeta* meta = reinterpret_cast<TileMeta*>(smem + L::kMeta);
   int* cols = reinterpret_cast<int*>(smem + L::kCols);
-
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int T = static_cast<int>(p.T);
   const int BM = p.block_m;
-  const uint64_t tmo = p.timeout_ns;
-
+  const Sync sy{bars, abort_flag, p.timeout_ns, &p.ws->error_word, lane};
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&bars[kKFull + i], 1);
@@ -359,8 +434,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kDrain], 1);
     *abort_flag = 0;
     mbar_fence_init();
-  }
-  if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tq);
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
@@ -373,35 +446,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-
-  auto fail = [&]() {
-    *abort_flag = 1;
-    atomicOr(&p.ws->error_word, static_cast<int>(FM_DEVERR_TIMEOUT));
-  };
-  // every lane waits; the warp proceeds only if all lanes saw the phase
-  auto warp_wait = [&](int bar, uint32_t parity) -> bool {
-    const bool ok = mbar_wait_bounded(&bars[bar], parity, tmo, abort_flag);
-    const bool all = __all_sync(0xffffffffu, ok);
-    if (!all && lane == 0) fail();
-    return all;
-  };
-  // single-thread wait
-  auto lone_wait = [&](int bar, uint32_t parity) -> bool {
-    if (mbar_wait_bounded(&bars[bar], parity, tmo, abort_flag)) return true;
-    fail();
-    return false;
-  };
-
-  // Each role below ends with teardown().
-  auto teardown = [&]() {
-    tc_fence_before();
-    asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
-    if (warp == 1) {
-      __syncwarp();
-      tc_fence_after();
-      tmem_dealloc(*reinterpret_cast<volatile uint32_t*>(tmem_slot), L::kTmemCols);
-    }
-  };
 
   if (warp == 0) {
     // --------------------------------------------------- K producer + metadata
@@ -417,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     auto push_meta = [&](int flags, int cls0, int cls1, int c0, int c1, int r0, int r_end, int h,
                          int kvh, bool copy_cols, int mh) -> bool {
-      if (!warp_wait(kMEmpty + mslot, (mround & 1) ^ 1)) return false;
+      if (!sy.warp(kMEmpty + mslot, (mround & 1) ^ 1)) return false;
       if (copy_cols) {
         const int32_t* src = p.sri + static_cast<int64_t>(mh) * 4 * p.T;
         int* dst = cols + mslot * 4 * BN;
@@ -552,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (pushed == 0) {
             // Q tiles of this item, once the previous item's S MMAs are done
-            if (!warp_wait(kQEmpty, (q_round & 1) ^ 1)) {
+            if (!sy.warp(kQEmpty, (q_round & 1) ^ 1)) {
               ok = false;
               break;
             }
@@ -572,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             q_armed = q_round;
             ++q_round;
           }
-          if (!warp_wait(kKEmpty + kst, (kround & 1) ^ 1)) {
+          if (!sy.warp(kKEmpty + kst, (kround & 1) ^ 1)) {
             ok = false;
             break;
           }
@@ -608,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       atomicAdd(reinterpret_cast<unsigned long long*>(p.class_counts + 2),
                 static_cast<unsigned long long>(cnt_u));
     }
-    teardown();
+    attn_teardown<D, BN>(tmem_slot, warp);
     return;
   } else if (warp == 2) {
     // --------------------------------------------------------------- V producer
@@ -617,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t v_armed[kStages] = {0xffffffffu, 0xffffffffu};
       bool ok = true;
       for (;;) {
-        if (!lone_wait(kMFull + mslot, mround & 1)) { ok = false; break; }
+        if (!sy.lone(kMFull + mslot, mround & 1)) { ok = false; break; }
         const int flags = *reinterpret_cast<volatile int*>(&meta[mslot].flags);
         const int c0 = *reinterpret_cast<volatile int*>(&meta[mslot].c0);
         const int kvh = *reinterpret_cast<volatile int*>(&meta[mslot].kvh);
@@ -627,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++mround;
         }
         if (flags & kStop) break;
-        if (!lone_wait(kVEmpty + vst, (vround & 1) ^ 1)) { ok = false; break; }
+        if (!sy.lone(kVEmpty + vst, (vround & 1) ^ 1)) { ok = false; break; }
         mbar_arrive_expect_tx(&bars[kVFull + vst], L::kVBytes);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
@@ -645,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_bounded(&bars[kVFull + st], v_armed[st] & 1, 100000000ull, nullptr);
       }
     }
-    teardown();
+    attn_teardown<D, BN>(tmem_slot, warp);
     return;
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -663,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
 
       auto next_flags = [&](int& flags) -> bool {
-        if (!lone_wait(kMFull + mslot, mround & 1)) return false;
+        if (!sy.lone(kMFull + mslot, mround & 1)) return false;
         flags = *reinterpret_cast<volatile int*>(&meta[mslot].flags);
         if (++mslot == kMetaSlots) {
           mslot = 0;
@@ -699,9 +743,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // S MMAs of the first tile of an item (waits for its Q tiles and K)
       auto start_item = [&](int flags) -> bool {
-        if (!lone_wait(kQFull, q_round & 1)) return false;
+        if (!sy.lone(kQFull, q_round & 1)) return false;
         ++q_round;
-        if (!lone_wait(kKFull + kst, kround & 1)) return false;
+        if (!sy.lone(kKFull + kst, kround & 1)) return false;
         tc_fence_after();
         issue_s(0);
         if (flags & kHasQ1) issue_s(1);
@@ -715,11 +759,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto wait_pv_ready = [&](int i, bool first) -> bool {
         if (first && o_pending[i]) {
-          if (!lone_wait(kOEmpty + i, o_round[i] & 1)) return false;
+          if (!sy.lone(kOEmpty + i, o_round[i] & 1)) return false;
           ++o_round[i];
           o_pending[i] = false;
         }
-        if (!lone_wait(kPFull + i, p_round[i] & 1)) return false;
+        if (!sy.lone(kPFull + i, p_round[i] & 1)) return false;
         ++p_round[i];
         tc_fence_after();
         return true;
@@ -734,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool q1 = (cur & kHasQ1) != 0;
         int nxt = 0;
         if (!last && !next_flags(nxt)) { ok = false; break; }
-        if (!lone_wait(kVFull + vst, vround & 1)) { ok = false; break; }
+        if (!sy.lone(kVFull + vst, vround & 1)) { ok = false; break; }
         // tile 0: PV, then S of the next KV tile (P_0 is read before S_0 is
         // overwritten: MMAs from one thread run in issue order)
         if (!wait_pv_ready(0, first)) { ok = false; break; }
@@ -744,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           o_pending[0] = true;
         }
         if (!last) {
-          if (!lone_wait(kKFull + kst, kround & 1)) { ok = false; break; }
+          if (!sy.lone(kKFull + kst, kround & 1)) { ok = false; break; }
           tc_fence_after();
           issue_s(0);
         }
@@ -781,9 +825,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(&bars[kDrain]);
       mbar_wait_bounded(&bars[kDrain], 0, 100000000ull, nullptr);
     }
-    teardown();
+    attn_teardown<D, BN>(tmem_slot, warp);
     return;
   } else {
+    attn_teardown<D, BN>(tmem_slot, warp);  // idle warp
+  }
+}
+
+// Warps 4..11 (raised register budget): softmax of Q tile 0 (warps 4..7) and
+// of Q tile 1 (warps 8..11).
+template <int D, int BN, typename IdxT>
+__device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
+  using L = Layout<D, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
+  TileMeta* meta = reinterpret_cast<TileMeta*>(smem + L::kMeta);
+  int* cols = reinterpret_cast<int*>(smem + L::kCols);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int T = static_cast<int>(p.T);
+  const int BM = p.block_m;
+  const Sync sy{bars, abort_flag, p.timeout_ns, &p.ws->error_word, lane};
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  {
     // ------------------------------------------------------------------ softmax
     const int wg = (warp - kFirstSoftmaxWarp) >> 2;  // which Q tile of the item
     const int row = (warp & 3) * 32 + lane;
@@ -799,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int rt0 = 0, rt1 = 0, h = 0;
 
     for (;;) {
-      if (!warp_wait(kMFull + mslot, mround & 1)) break;
+      if (!sy.warp(kMFull + mslot, mround & 1)) break;
       const TileMeta* mp = meta + mslot;
       const int flags = *reinterpret_cast<const volatile int*>(&mp->flags);
       if (flags & kStop) break;
@@ -829,7 +900,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_run = -CUDART_INF_F;
         l_run = 0.f;
       }
-      if (!warp_wait(kSFull + wg, s_round & 1)) break;
+      if (!sy.warp(kSFull + wg, s_round & 1)) break;
       ++s_round;
       tc_fence_after();
 
@@ -872,30 +943,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < BN / 32; ++c) tmem_st16(s_tmem + c * 16, z);
         tmem_st_wait();
       } else {
-        // pass 1: row max, 64 columns per TMEM load
+        // the whole S row in registers: one TMEM load, one wait
+        uint32_t sr[BN];
+        tmem_ld_row<BN>(s_tmem, sr);
         float m8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) m8[i] = -CUDART_INF_F;
+        if (cls == kClsP) {
 #pragma unroll
-        for (int h64 = 0; h64 < BN / 64; ++h64) {
-          uint32_t sr[64];
-          tmem_ld64(s_tmem + h64 * 64, sr);
-          if (cls == kClsP) {
-            const uint32_t b0 = mbits[2 * h64], b1 = mbits[2 * h64 + 1];
-#pragma unroll
-            for (int j = 0; j < 64; ++j) {
-              const bool masked = ((j < 32 ? b0 >> j : b1 >> (j - 32)) & 1u) != 0u;
-              m8[j & 7] = fmaxf(m8[j & 7], masked ? -CUDART_INF_F : __uint_as_float(sr[j]));
-            }
-          } else if (valid < BN) {
-#pragma unroll
-            for (int j = 0; j < 64; ++j)
-              m8[j & 7] = fmaxf(m8[j & 7],
-                                h64 * 64 + j >= valid ? -CUDART_INF_F : __uint_as_float(sr[j]));
-          } else {
-#pragma unroll
-            for (int j = 0; j < 64; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j]));
+          for (int j = 0; j < BN; ++j) {
+            if ((mbits[j >> 5] >> (j & 31)) & 1u) sr[j] = __float_as_uint(-CUDART_INF_F);
+            m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j]));
           }
+        } else if (valid < BN) {
+#pragma unroll
+          for (int j = 0; j < BN; ++j) {
+            if (j >= valid) sr[j] = __float_as_uint(-CUDART_INF_F);
+            m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j]));
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < BN; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j]));
         }
         const float mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
@@ -918,37 +986,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         float sum8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) sum8[i] = 0.f;
-        // pass 2: P = 2^(x - m), 64 columns per TMEM load; P overwrites the
-        // first half of the S columns (already consumed)
+        // P = 2^(x - m) as bf16 into the first half of the S columns
 #pragma unroll
-        for (int h64 = 0; h64 < BN / 64; ++h64) {
-          uint32_t sr[64];
-          tmem_ld64(s_tmem + h64 * 64, sr);
-          if (cls == kClsP) {
-            const uint32_t b0 = mbits[2 * h64], b1 = mbits[2 * h64 + 1];
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-              const bool masked = ((j < 32 ? b0 >> j : b1 >> (j - 32)) & 1u) != 0u;
-              if (masked) sr[j] = __float_as_uint(-CUDART_INF_F);
-            }
-          } else if (valid < BN) {
-#pragma unroll
-            for (int j = 0; j < 64; ++j)
-              if (h64 * 64 + j >= valid) sr[j] = __float_as_uint(-CUDART_INF_F);
+          for (int i = 0; i < 32; i += 2) {
+            const int j = c * 32 + i;
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[j]), scale_log2, neg_base));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[j + 1]), scale_log2, neg_base));
+            sum8[(i >> 1) & 7] += p0 + p1;
+            pk[i >> 1] = pack_bf16x2(p0, p1);
           }
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const int j = c * 32 + i;
-              const float p0 = ex2_approx(fmaf(__uint_as_float(sr[j]), scale_log2, neg_base));
-              const float p1 = ex2_approx(fmaf(__uint_as_float(sr[j + 1]), scale_log2, neg_base));
-              sum8[(i >> 1) & 7] += p0 + p1;
-              pk[i >> 1] = pack_bf16x2(p0, p1);
-            }
-            tmem_st16(s_tmem + h64 * 32 + c * 16, pk);
-          }
+          tmem_st16(s_tmem + c * 16, pk);
         }
         tmem_st_wait();
         l_run += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
@@ -972,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bars[kPFull + wg]);
 
       if (flags & kLast) {
-        if (!warp_wait(kOFull + wg, o_round & 1)) break;
+        if (!sy.warp(kOFull + wg, o_round & 1)) break;
         ++o_round;
         tc_fence_after();
         const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
@@ -1006,8 +1056,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars[kOEmpty + wg]);
       }
     }
-    teardown();
-    return;
+    attn_teardown<D, BN>(tmem_slot, warp);
+  }
+}
+
+template <int D, int BN, typename IdxT>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tq,
+                    const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv) {
+  // The register split comes first so that no value crosses from one budget
+  // into the other.
+  if ((threadIdx.x >> 5) < 4) {
+    regs_release();
+    attn_producer_roles<D, BN, IdxT>(p, tq, tk, tv);
+  } else {
+    regs_acquire();
+    attn_softmax_role<D, BN, IdxT>(p);
   }
 }
 
@@ -1033,6 +1098,13 @@ cudaError_t launch_typed(const AttnParams& p, const CUtensorMap& tq, const CUten
   if (e != cudaSuccess) return e;
   static unsigned long long configured = 0ull;  // one bit per device; setting twice is harmless
   if (dev >= 64 || !((configured >> dev) & 1ull)) {
+    // The warpgroups' register split must fit in what the launch allocates,
+    // or setmaxnreg.inc would wait forever: refuse to launch otherwise.
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, attn_fwd_kernel<D, BN, IdxT>);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs * kThreads < kProducerRegs * 128 + kSoftmaxRegs * 256)
+      return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(attn_fwd_kernel<D, BN, IdxT>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
