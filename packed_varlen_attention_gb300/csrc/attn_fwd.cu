@@ -64,7 +64,11 @@ constexpr int kTileM = 128;  // MMA M: TMEM lanes = tile rows
 constexpr int kMetaSlots = 4;
 constexpr int kPrefetchAhead = 3;  // K/V tiles pulled into L2 ahead of their loads
 
-enum : int { kClsF = 0, kClsP = 1, kClsU = 2 };
+// kClsP: partially masked through the column intervals (element mask from the
+// four vectors); kClsPC: partially masked only through causality and the
+// sample bound (the diagonal block of a causal mask).  Both count as
+// partially masked.
+enum : int { kClsF = 0, kClsP = 1, kClsU = 2, kClsPC = 3 };
 enum : int { kFirst = 1, kLast = 2, kHasQ1 = 4, kStop = 8 };
 
 struct TileMeta {
@@ -136,7 +140,8 @@ __device__ __forceinline__ int classify_block(int r0, int r1, int c0, int c1, co
   if (r1 - 1 < c0) return ut_full ? kClsF : (ut_touch ? kClsP : kClsU);
   if (r0 >= c1 - 1) return lt_full ? kClsF : (lt_touch ? kClsP : kClsU);
   if (lt_full && ut_full) return kClsF;
-  if (causal || lt_touch || ut_touch) return kClsP;
+  if (lt_touch || (!causal && ut_touch)) return kClsP;
+  if (causal) return kClsPC;  // only the diagonal (and no interval) masks it
   return kClsU;
 }
 
@@ -322,6 +327,151 @@ __device__ __forceinline__ void tmem_ld_row<64>(uint32_t taddr, uint32_t (&r)[64
 template <>
 __device__ __forceinline__ void tmem_ld_row<128>(uint32_t taddr, uint32_t (&r)[128]) {
   tmem_ld128(taddr, r);
+}
+
+// Groups of MMAs issued from one asm block: the issuing thread spends no
+// instructions between consecutive tcgen05.mma but two descriptor adds (the
+// issue of each MMA is paced by the tensor pipe itself).  The first step
+// accumulates iff acc0 != 0, the later ones always accumulate.
+// SS: A and B from shared memory, step k adds OA_k / OB_k to the descriptors'
+// start-address fields.  TS: A from TMEM (8 columns per K=16 step), B from
+// shared memory advanced by OB per step.
+template <int OA1, int OB1, int OA2, int OB2, int OA3, int OB3>
+__device__ __forceinline__ void umma_ss_group4(uint32_t d_tmem, uint64_t a_desc,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t acc0) {
+  asm volatile("{\n\t.reg .pred p, q;\n\t.reg .b64 a, b;\n\t"
+               "setp.ne.b32 p, %4, 0;\n\t"
+               "setp.eq.u32 q, 0, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+               "add.s64 a, %1, %5;\n\tadd.s64 b, %2, %6;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "add.s64 a, %1, %7;\n\tadd.s64 b, %2, %8;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "add.s64 a, %1, %9;\n\tadd.s64 b, %2, %10;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "}"
+               :: "r"(d_tmem),
+                  "l"(a_desc),
+                  "l"(b_desc),
+                  "r"(idesc),
+                  "r"(acc0),
+                  "n"(OA1),
+                  "n"(OB1),
+                  "n"(OA2),
+                  "n"(OB2),
+                  "n"(OA3),
+                  "n"(OB3)
+               : "memory");
+}
+
+template <int OA1, int OB1, int OA2, int OB2, int OA3, int OB3, int OA4, int OB4, int OA5, int OB5, int OA6, int OB6, int OA7, int OB7>
+__device__ __forceinline__ void umma_ss_group8(uint32_t d_tmem, uint64_t a_desc,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t acc0) {
+  asm volatile("{\n\t.reg .pred p, q;\n\t.reg .b64 a, b;\n\t"
+               "setp.ne.b32 p, %4, 0;\n\t"
+               "setp.eq.u32 q, 0, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+               "add.s64 a, %1, %5;\n\tadd.s64 b, %2, %6;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "add.s64 a, %1, %7;\n\tadd.s64 b, %2, %8;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "add.s64 a, %1, %9;\n\tadd.s64 b, %2, %10;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "add.s64 a, %1, %11;\n\tadd.s64 b, %2, %12;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "add.s64 a, %1, %13;\n\tadd.s64 b, %2, %14;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "add.s64 a, %1, %15;\n\tadd.s64 b, %2, %16;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "add.s64 a, %1, %17;\n\tadd.s64 b, %2, %18;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "}"
+               :: "r"(d_tmem),
+                  "l"(a_desc),
+                  "l"(b_desc),
+                  "r"(idesc),
+                  "r"(acc0),
+                  "n"(OA1),
+                  "n"(OB1),
+                  "n"(OA2),
+                  "n"(OB2),
+                  "n"(OA3),
+                  "n"(OB3),
+                  "n"(OA4),
+                  "n"(OB4),
+                  "n"(OA5),
+                  "n"(OB5),
+                  "n"(OA6),
+                  "n"(OB6),
+                  "n"(OA7),
+                  "n"(OB7)
+               : "memory");
+}
+
+template <int OB>
+__device__ __forceinline__ void umma_ts_group4(uint32_t d_tmem, uint32_t a_tmem,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t acc0) {
+  asm volatile("{\n\t.reg .pred p, q;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+               "setp.ne.b32 p, %4, 0;\n\t"
+               "setp.eq.u32 q, 0, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+               "add.u32 a, %1, 8;\n\tadd.s64 b, %2, %5;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "add.u32 a, %1, 16;\n\tadd.s64 b, %2, %6;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "add.u32 a, %1, 24;\n\tadd.s64 b, %2, %7;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "}"
+               :: "r"(d_tmem),
+                  "r"(a_tmem),
+                  "l"(b_desc),
+                  "r"(idesc),
+                  "r"(acc0),
+                  "n"(1 * OB),
+                  "n"(2 * OB),
+                  "n"(3 * OB)
+               : "memory");
+}
+
+template <int OB>
+__device__ __forceinline__ void umma_ts_group8(uint32_t d_tmem, uint32_t a_tmem,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t acc0) {
+  asm volatile("{\n\t.reg .pred p, q;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+               "setp.ne.b32 p, %4, 0;\n\t"
+               "setp.eq.u32 q, 0, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+               "add.u32 a, %1, 8;\n\tadd.s64 b, %2, %5;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "add.u32 a, %1, 16;\n\tadd.s64 b, %2, %6;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "add.u32 a, %1, 24;\n\tadd.s64 b, %2, %7;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "add.u32 a, %1, 32;\n\tadd.s64 b, %2, %8;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "add.u32 a, %1, 40;\n\tadd.s64 b, %2, %9;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "add.u32 a, %1, 48;\n\tadd.s64 b, %2, %10;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "add.u32 a, %1, 56;\n\tadd.s64 b, %2, %11;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "}"
+               :: "r"(d_tmem),
+                  "r"(a_tmem),
+                  "l"(b_desc),
+                  "r"(idesc),
+                  "r"(acc0),
+                  "n"(1 * OB),
+                  "n"(2 * OB),
+                  "n"(3 * OB),
+                  "n"(4 * OB),
+                  "n"(5 * OB),
+                  "n"(6 * OB),
+                  "n"(7 * OB)
+               : "memory");
 }
 
 // Register split between the warpgroups (all four warps of a warpgroup run
@@ -525,9 +675,9 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         int c0, c1;
         tile_classes<BN>(p, mh, s, a, b, r0, r1, r2, base + lane, kt_end, c0, c1);
         n_live += __popc(__ballot_sync(0xffffffffu, c0 != kClsF || c1 != kClsF));
-        const int p0 = __popc(__ballot_sync(0xffffffffu, c0 == kClsP));
+        const int p0 = __popc(__ballot_sync(0xffffffffu, c0 == kClsP || c0 == kClsPC));
         const int u0 = __popc(__ballot_sync(0xffffffffu, c0 == kClsU));
-        const int p1 = __popc(__ballot_sync(0xffffffffu, c1 == kClsP));
+        const int p1 = __popc(__ballot_sync(0xffffffffu, c1 == kClsP || c1 == kClsPC));
         const int u1 = __popc(__ballot_sync(0xffffffffu, c1 == kClsU));
         cnt_p += p0 + p1;
         cnt_u += u0 + u1;
@@ -715,18 +865,24 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         }
         return true;
       };
+      // Shared-memory descriptors are built once; an MMA step only adds a
+      // constant to the start-address field (14 bits of addr >> 4, which no
+      // offset inside the tile can overflow).
+      const uint64_t q_desc0 = sdesc_sw128(q_addr, 16, 1024);
+      const uint64_t k_desc0 = sdesc_sw128(k_addr, 16, 1024);
+      const uint64_t v_desc0 = sdesc_sw128(v_addr, BN * 128, 1024);
       // S_i = Q_i K^T for the K tile in stage kst
       auto issue_s = [&](int i) {
         const uint32_t d_tmem = tmem_base + i * 128;
-        const uint32_t qa = q_addr + i * L::kQBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk & 3) * 32;
-          const uint32_t chunk = kk >> 2;
-          const uint64_t ad = sdesc_sw128(qa + chunk * (kTileM * 128) + koff, 16, 1024);
-          const uint64_t bd =
-              sdesc_sw128(k_addr + kst * L::kKBytes + chunk * (BN * 128) + koff, 16, 1024);
-          umma_bf16(d_tmem, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+        const uint64_t qd = q_desc0 + static_cast<uint64_t>(i * (L::kQBytes >> 4));
+        const uint64_t kd = k_desc0 + static_cast<uint64_t>(kst * (L::kKBytes >> 4));
+        constexpr int QC = (kTileM * 128) >> 4;  // next 64-column chunk of Q
+        constexpr int KC = (BN * 128) >> 4;      // next 64-column chunk of K
+        if constexpr (D == 128) {
+          umma_ss_group8<2, 2, 4, 4, 6, 6, QC, KC, QC + 2, KC + 2, QC + 4, KC + 4, QC + 6, KC + 6>(
+              d_tmem, qd, kd, kIdescS, 0u);
+        } else {
+          umma_ss_group4<2, 2, 4, 4, 6, 6>(d_tmem, qd, kd, kIdescS, 0u);
         }
         umma_commit(&bars[kSFull + i]);
       };
@@ -734,11 +890,12 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       auto issue_pv = [&](int i, bool first) {
         const uint32_t d_tmem = tmem_base + 256 + i * 128;
         const uint32_t a_tmem = tmem_base + i * 128;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bd =
-              sdesc_sw128(v_addr + vst * L::kVBytes + kk * (16 * 128), BN * 128, 1024);
-          umma_bf16_tmem_a(d_tmem, a_tmem + kk * 8, bd, kIdescO, (!first || kk > 0) ? 1u : 0u);
+        const uint64_t vd = v_desc0 + static_cast<uint64_t>(vst * (L::kVBytes >> 4));
+        constexpr int VS = (16 * 128) >> 4;  // 16 rows of V per K=16 step
+        if constexpr (BN == 128) {
+          umma_ts_group8<VS>(d_tmem, a_tmem, vd, kIdescO, first ? 0u : 1u);
+        } else {
+          umma_ts_group4<VS>(d_tmem, a_tmem, vd, kIdescO, first ? 0u : 1u);
         }
       };
       // S MMAs of the first tile of an item (waits for its Q tiles and K)
@@ -777,7 +934,6 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         const bool last = (cur & kLast) != 0;
         const bool q1 = (cur & kHasQ1) != 0;
         int nxt = 0;
-        if (!last && !next_flags(nxt)) { ok = false; break; }
         if (!sy.lone(kVFull + vst, vround & 1)) { ok = false; break; }
         // tile 0: PV, then S of the next KV tile (P_0 is read before S_0 is
         // overwritten: MMAs from one thread run in issue order)
@@ -790,6 +946,12 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         if (!last) {
           if (!sy.lone(kKFull + kst, kround & 1)) { ok = false; break; }
           tc_fence_after();
+          // the metadata of this K tile was written before its load was armed
+          nxt = *reinterpret_cast<volatile int*>(&meta[mslot].flags);
+          if (++mslot == kMetaSlots) {
+            mslot = 0;
+            ++mround;
+          }
           issue_s(0);
         }
         // tile 1
@@ -862,7 +1024,6 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
     const uint32_t s_tmem = tmem_base + lane_addr + wg * 128;
     const uint32_t o_tmem = tmem_base + lane_addr + 256 + wg * 128;
     const float scale_log2 = p.scale_log2;
-    const bool has_mask = p.sri != nullptr;
     const bool causal = p.causal != 0;
     uint32_t mslot = 0, mround = 0;
     uint32_t s_round = 0, o_round = 0;
@@ -907,25 +1068,44 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
       const int r = rt0 + row;
       const int valid = c1 - c0;  // columns inside the sample
       uint32_t mbits[BN / 32];    // element mask of a partially masked block
-      if (cls == kClsP) {
-        // element mask of the row as bits, before any score is loaded
+      if (cls == kClsPC) {
+        // causal diagonal: column c0 + jj is masked iff it lies above row r
+        // or outside the sample; 32 columns at a time with shifts
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          const int d = r - (c0 + c * 32);  // columns jj - 32c > d are above the row
+          const uint32_t above = d >= 31 ? 0u : (d < 0 ? 0xffffffffu : (0xffffffffu << (d + 1)));
+          const int v = valid - c * 32;     // columns from v on are outside the sample
+          const uint32_t out = v >= 32 ? 0u : (v <= 0 ? 0xffffffffu : (0xffffffffu << v));
+          mbits[c] = above | out;
+        }
+      } else if (cls == kClsP) {
+        // column intervals: row r is masked in column j iff it lies in
+        // [LTS_j, LTE_j) on or below the diagonal, or above the diagonal and
+        // (causal or in [UTS_j, UTE_j)); branch-free, four columns per load
         const int* cl = cols + cur_slot * 4 * BN;
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t bits = 0;
-#pragma unroll 4
-          for (int i = 0; i < 32; ++i) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
             const int jj = c * 32 + i;
-            const int col = c0 + jj;
-            bool masked;
-            if (jj >= valid) {
-              masked = true;
-            } else if (r >= col) {
-              masked = has_mask && (cl[jj] <= r) && (r < cl[BN + jj]);
-            } else {
-              masked = causal || (has_mask && (cl[2 * BN + jj] <= r) && (r < cl[3 * BN + jj]));
+            const int4 lts = *reinterpret_cast<const int4*>(cl + jj);
+            const int4 lte = *reinterpret_cast<const int4*>(cl + BN + jj);
+            const int4 uts = *reinterpret_cast<const int4*>(cl + 2 * BN + jj);
+            const int4 ute = *reinterpret_cast<const int4*>(cl + 3 * BN + jj);
+            const int a[4] = {lts.x, lts.y, lts.z, lts.w};
+            const int e[4] = {lte.x, lte.y, lte.z, lte.w};
+            const int ua[4] = {uts.x, uts.y, uts.z, uts.w};
+            const int ue[4] = {ute.x, ute.y, ute.z, ute.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const bool lower = r >= c0 + jj + t;
+              const bool in_lt = (a[t] <= r) & (r < e[t]);
+              const bool in_ut = causal | ((ua[t] <= r) & (r < ue[t]));
+              const bool m = (jj + t >= valid) | (lower ? in_lt : in_ut);
+              bits |= static_cast<uint32_t>(m) << (i + t);
             }
-            bits |= (masked ? 1u : 0u) << i;
           }
           mbits[c] = bits;
         }
@@ -949,7 +1129,7 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
         float m8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) m8[i] = -CUDART_INF_F;
-        if (cls == kClsP) {
+        if (cls == kClsP || cls == kClsPC) {
 #pragma unroll
           for (int j = 0; j < BN; ++j) {
             if ((mbits[j >> 5] >> (j & 31)) & 1u) sr[j] = __float_as_uint(-CUDART_INF_F);

@@ -56,19 +56,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase of parity `parity` to complete.  Gives up after
-// `timeout_ns` of wall time, or as soon as *abort becomes nonzero (another
-// role of the CTA gave up), and then returns false.  Never spins forever.
+// Bounded wait: never spins forever (see the comment inside).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   uint64_t timeout_ns,
                                                   volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (abort != nullptr && *abort != 0) return false;
-    if (global_timer_ns() - t0 > timeout_ns) return false;
-  }
+  // Waits for the phase of parity `parity`; gives up after `timeout_ns` of
+  // wall time or as soon as *abort (shared memory) becomes nonzero, and then
+  // returns false.  One asm block: when the phase is already complete this
+  // costs a single try_wait and a predicated branch.
+  const uint32_t abort_addr = abort != nullptr ? smem_u32(const_cast<int*>(abort)) : 0u;
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .u64 t0, t1;\n\t.reg .u32 ab;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "@p bra FM_WDONE_%=;\n\t"
+      "mov.u64 t0, %%globaltimer;\n"
+      "FM_WLOOP_%=:\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "@p bra FM_WDONE_%=;\n\t"
+      "setp.ne.u32 q, %3, 0;\n\t"
+      "@!q bra FM_WTIME_%=;\n\t"
+      "ld.volatile.shared.u32 ab, [%3];\n\t"
+      "setp.ne.u32 q, ab, 0;\n\t"
+      "@q bra FM_WDONE_%=;\n"
+      "FM_WTIME_%=:\n\t"
+      "mov.u64 t1, %%globaltimer;\n\t"
+      "sub.u64 t1, t1, t0;\n\t"
+      "setp.gt.u64 q, t1, %4;\n\t"
+      "@!q bra FM_WLOOP_%=;\n"
+      "FM_WDONE_%=:\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(abort_addr), "l"(timeout_ns)
+      : "memory");
+  return ok != 0;
 }
 
 // ---------------------------------------------------------------------------
