@@ -161,6 +161,25 @@ class ClockSampler:
                 "power_w_max": float(max(power))}
 
 
+def measured_traffic():
+    """DRAM bytes per attention launch from the committed ncu capture, or None
+    when the kernel source changed since that capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "attn_fwd_dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        h = hashlib.sha256()
+        for src in d["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as g:
+                h.update(g.read())
+        if h.hexdigest() != d["source_sha256"]:
+            return None
+        return int(d["dram_bytes_read"]) + int(d["dram_bytes_write"])
+    except (OSError, ValueError, KeyError):
+        return None
+
+
 def dist_info():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -408,7 +427,8 @@ def run_ours(args):
             "unit": "TFLOP/s",
             "frac": attn_tflops / peaks["bf16_tflops"],
             "peak_source": f"{peak_src} bf16 burst",
-            "traffic": None,
+            "traffic": measured_traffic(),
+            "traffic_unit": "bytes per launch (ncu dram read + write, headline workload)",
         },
         "rope": {"bound": "hbm", "achieved": rope_gbs, "unit": "GB/s",
                  "peak": peaks["hbm_gbs"], "frac": rope_gbs / peaks["hbm_gbs"],
