@@ -329,10 +329,13 @@ __device__ __forceinline__ void tmem_ld_row<128>(uint32_t taddr, uint32_t (&r)[1
   tmem_ld128(taddr, r);
 }
 
-// Groups of MMAs issued from one asm block: the issuing thread spends no
-// instructions between consecutive tcgen05.mma but two descriptor adds (the
-// issue of each MMA is paced by the tensor pipe itself).  The first step
-// accumulates iff acc0 != 0, the later ones always accumulate.
+// Groups of MMAs issued from one asm block by the converged warp: every lane
+// runs the block and elect.sync picks the one that issues.  Issue from a
+// warp-uniform stream costs far fewer issue cycles than the same MMAs issued
+// by lane 0 inside a divergent branch, and keeps up with the tensor pipe
+// when softmax warps share the issuer's SMSP.  Between consecutive MMAs the
+// issuing lane only adds two descriptor offsets.  The first step accumulates
+// iff acc0 != 0, the later ones always accumulate.
 // SS: A and B from shared memory, step k adds OA_k / OB_k to the descriptors'
 // start-address fields.  TS: A from TMEM (8 columns per K=16 step), B from
 // shared memory advanced by OB per step.
@@ -340,16 +343,18 @@ template <int OA1, int OB1, int OA2, int OB2, int OA3, int OB3>
 __device__ __forceinline__ void umma_ss_group4(uint32_t d_tmem, uint64_t a_desc,
                                                  uint64_t b_desc, uint32_t idesc,
                                                  uint32_t acc0) {
-  asm volatile("{\n\t.reg .pred p, q;\n\t.reg .b64 a, b;\n\t"
+  asm volatile("{\n\t.reg .pred p, q, e;\n\t.reg .b32 el;\n\t"
+               ".reg .b64 a, b;\n\t"
+               "elect.sync el|e, 0xffffffff;\n\t"
                "setp.ne.b32 p, %4, 0;\n\t"
                "setp.eq.u32 q, 0, 0;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
                "add.s64 a, %1, %5;\n\tadd.s64 b, %2, %6;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
                "add.s64 a, %1, %7;\n\tadd.s64 b, %2, %8;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
                "add.s64 a, %1, %9;\n\tadd.s64 b, %2, %10;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
                "}"
                :: "r"(d_tmem),
                   "l"(a_desc),
@@ -369,24 +374,26 @@ template <int OA1, int OB1, int OA2, int OB2, int OA3, int OB3, int OA4, int OB4
 __device__ __forceinline__ void umma_ss_group8(uint32_t d_tmem, uint64_t a_desc,
                                                  uint64_t b_desc, uint32_t idesc,
                                                  uint32_t acc0) {
-  asm volatile("{\n\t.reg .pred p, q;\n\t.reg .b64 a, b;\n\t"
+  asm volatile("{\n\t.reg .pred p, q, e;\n\t.reg .b32 el;\n\t"
+               ".reg .b64 a, b;\n\t"
+               "elect.sync el|e, 0xffffffff;\n\t"
                "setp.ne.b32 p, %4, 0;\n\t"
                "setp.eq.u32 q, 0, 0;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
                "add.s64 a, %1, %5;\n\tadd.s64 b, %2, %6;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
                "add.s64 a, %1, %7;\n\tadd.s64 b, %2, %8;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
                "add.s64 a, %1, %9;\n\tadd.s64 b, %2, %10;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
                "add.s64 a, %1, %11;\n\tadd.s64 b, %2, %12;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
                "add.s64 a, %1, %13;\n\tadd.s64 b, %2, %14;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
                "add.s64 a, %1, %15;\n\tadd.s64 b, %2, %16;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
                "add.s64 a, %1, %17;\n\tadd.s64 b, %2, %18;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
                "}"
                :: "r"(d_tmem),
                   "l"(a_desc),
@@ -414,16 +421,18 @@ template <int OB>
 __device__ __forceinline__ void umma_ts_group4(uint32_t d_tmem, uint32_t a_tmem,
                                                  uint64_t b_desc, uint32_t idesc,
                                                  uint32_t acc0) {
-  asm volatile("{\n\t.reg .pred p, q;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+  asm volatile("{\n\t.reg .pred p, q, e;\n\t.reg .b32 el;\n\t"
+               ".reg .b64 b;\n\t.reg .b32 a;\n\t"
+               "elect.sync el|e, 0xffffffff;\n\t"
                "setp.ne.b32 p, %4, 0;\n\t"
                "setp.eq.u32 q, 0, 0;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
                "add.u32 a, %1, 8;\n\tadd.s64 b, %2, %5;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
                "add.u32 a, %1, 16;\n\tadd.s64 b, %2, %6;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
                "add.u32 a, %1, 24;\n\tadd.s64 b, %2, %7;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
                "}"
                :: "r"(d_tmem),
                   "r"(a_tmem),
@@ -440,24 +449,26 @@ template <int OB>
 __device__ __forceinline__ void umma_ts_group8(uint32_t d_tmem, uint32_t a_tmem,
                                                  uint64_t b_desc, uint32_t idesc,
                                                  uint32_t acc0) {
-  asm volatile("{\n\t.reg .pred p, q;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+  asm volatile("{\n\t.reg .pred p, q, e;\n\t.reg .b32 el;\n\t"
+               ".reg .b64 b;\n\t.reg .b32 a;\n\t"
+               "elect.sync el|e, 0xffffffff;\n\t"
                "setp.ne.b32 p, %4, 0;\n\t"
                "setp.eq.u32 q, 0, 0;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
                "add.u32 a, %1, 8;\n\tadd.s64 b, %2, %5;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
                "add.u32 a, %1, 16;\n\tadd.s64 b, %2, %6;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
                "add.u32 a, %1, 24;\n\tadd.s64 b, %2, %7;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
                "add.u32 a, %1, 32;\n\tadd.s64 b, %2, %8;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
                "add.u32 a, %1, 40;\n\tadd.s64 b, %2, %9;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
                "add.u32 a, %1, 48;\n\tadd.s64 b, %2, %10;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
                "add.u32 a, %1, 56;\n\tadd.s64 b, %2, %11;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
                "}"
                :: "r"(d_tmem),
                   "r"(a_tmem),
@@ -517,6 +528,19 @@ __device__ __forceinline__ void attn_teardown(uint32_t* tmem_slot, int warp) {
 
 // Bounded waits shared by every role; on expiry the CTA is told to stop and
 // FM_DEVERR_TIMEOUT is recorded.
+
+// tcgen05.commit from the lane elect.sync picks (the lane that issued the
+// MMAs: the whole warp is converged at every call, so the same lane is
+// elected each time).
+__device__ __forceinline__ void umma_commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 el;\n\t"
+      "elect.sync el|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
 struct Sync {
   uint64_t* bars;
   volatile int* abort;
@@ -843,7 +867,9 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
     return;
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop (every branch condition is warp-uniform);
+    // MMAs and commits are issued by the lane elect.sync picks.
+    {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kTileM, BN, false);
       constexpr uint32_t kIdescO = idesc_bf16_f32(kTileM, D, true);
       const uint32_t q_addr = smem_u32(smem + L::kQ);
@@ -857,7 +883,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       bool ok = true;
 
       auto next_flags = [&](int& flags) -> bool {
-        if (!sy.lone(kMFull + mslot, mround & 1)) return false;
+        if (!sy.warp(kMFull + mslot, mround & 1)) return false;
         flags = *reinterpret_cast<volatile int*>(&meta[mslot].flags);
         if (++mslot == kMetaSlots) {
           mslot = 0;
@@ -884,7 +910,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         } else {
           umma_ss_group4<2, 2, 4, 4, 6, 6>(d_tmem, qd, kd, kIdescS, 0u);
         }
-        umma_commit(&bars[kSFull + i]);
+        umma_commit_elect(&bars[kSFull + i]);
       };
       // O_i (+)= P_i V for the V tile in stage vst
       auto issue_pv = [&](int i, bool first) {
@@ -900,14 +926,14 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       };
       // S MMAs of the first tile of an item (waits for its Q tiles and K)
       auto start_item = [&](int flags) -> bool {
-        if (!sy.lone(kQFull, q_round & 1)) return false;
+        if (!sy.warp(kQFull, q_round & 1)) return false;
         ++q_round;
-        if (!sy.lone(kKFull + kst, kround & 1)) return false;
+        if (!sy.warp(kKFull + kst, kround & 1)) return false;
         tc_fence_after();
         issue_s(0);
         if (flags & kHasQ1) issue_s(1);
-        umma_commit(&bars[kKEmpty + kst]);
-        if (flags & kLast) umma_commit(&bars[kQEmpty]);
+        umma_commit_elect(&bars[kKEmpty + kst]);
+        if (flags & kLast) umma_commit_elect(&bars[kQEmpty]);
         if (++kst == kStages) {
           kst = 0;
           ++kround;
@@ -916,11 +942,11 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       };
       auto wait_pv_ready = [&](int i, bool first) -> bool {
         if (first && o_pending[i]) {
-          if (!sy.lone(kOEmpty + i, o_round[i] & 1)) return false;
+          if (!sy.warp(kOEmpty + i, o_round[i] & 1)) return false;
           ++o_round[i];
           o_pending[i] = false;
         }
-        if (!sy.lone(kPFull + i, p_round[i] & 1)) return false;
+        if (!sy.warp(kPFull + i, p_round[i] & 1)) return false;
         ++p_round[i];
         tc_fence_after();
         return true;
@@ -934,17 +960,17 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         const bool last = (cur & kLast) != 0;
         const bool q1 = (cur & kHasQ1) != 0;
         int nxt = 0;
-        if (!sy.lone(kVFull + vst, vround & 1)) { ok = false; break; }
+        if (!sy.warp(kVFull + vst, vround & 1)) { ok = false; break; }
         // tile 0: PV, then S of the next KV tile (P_0 is read before S_0 is
         // overwritten: MMAs from one thread run in issue order)
         if (!wait_pv_ready(0, first)) { ok = false; break; }
         issue_pv(0, first);
         if (last) {
-          umma_commit(&bars[kOFull + 0]);
+          umma_commit_elect(&bars[kOFull + 0]);
           o_pending[0] = true;
         }
         if (!last) {
-          if (!sy.lone(kKFull + kst, kround & 1)) { ok = false; break; }
+          if (!sy.warp(kKFull + kst, kround & 1)) { ok = false; break; }
           tc_fence_after();
           // the metadata of this K tile was written before its load was armed
           nxt = *reinterpret_cast<volatile int*>(&meta[mslot].flags);
@@ -959,19 +985,19 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
           if (!wait_pv_ready(1, first)) { ok = false; break; }
           issue_pv(1, first);
           if (last) {
-            umma_commit(&bars[kOFull + 1]);
+            umma_commit_elect(&bars[kOFull + 1]);
             o_pending[1] = true;
           }
           if (!last) issue_s(1);
         }
-        umma_commit(&bars[kVEmpty + vst]);
+        umma_commit_elect(&bars[kVEmpty + vst]);
         if (++vst == kStages) {
           vst = 0;
           ++vround;
         }
         if (!last) {
-          umma_commit(&bars[kKEmpty + kst]);
-          if (nxt & kLast) umma_commit(&bars[kQEmpty]);
+          umma_commit_elect(&bars[kKEmpty + kst]);
+          if (nxt & kLast) umma_commit_elect(&bars[kQEmpty]);
           if (++kst == kStages) {
             kst = 0;
             ++kround;
@@ -984,7 +1010,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         cur = nxt;
       }
       // all issued MMAs complete before TMEM is released
-      umma_commit(&bars[kDrain]);
+      umma_commit_elect(&bars[kDrain]);
       mbar_wait_bounded(&bars[kDrain], 0, 100000000ull, nullptr);
     }
     attn_teardown<D, BN>(tmem_slot, warp);
