@@ -64,6 +64,25 @@ constexpr int kTileM = 128;  // MMA M: TMEM lanes = tile rows
 constexpr int kMetaSlots = 4;
 constexpr int kPrefetchAhead = 3;  // K/V tiles pulled into L2 ahead of their loads
 
+// With 64-column key tiles TMEM holds two S buffers per Q tile (S_i of KV
+// tile t+2 is computed into the buffer PV_i of tile t has just read, while
+// the softmax works on tile t+1) and shared memory two Q buffers (the next
+// item's Q tiles land while the current item runs).  128-column key tiles
+// fill TMEM with one S per Q tile.
+template <int BN>
+constexpr int kBufs = (BN == 64) ? 2 : 1;
+
+// MMA issuing warps.  With one S buffer each Q tile has its own issuer (warps
+// 1 and 3), so one tile's barrier waits never hold up the other tile's MMAs;
+// with two S buffers warp 1 issues for both.
+template <int BN>
+constexpr int kIssuers = (BN == 64) ? 1 : 2;
+
+// One S buffer: hand S and P over in 64-column halves (the upper half of the
+// next S starts once the softmax holds S in registers, PV starts on the first
+// half of P) instead of whole tiles.
+constexpr bool kSplitHandoff = false;
+
 // kClsP: partially masked through the column intervals (element mask from the
 // four vectors); kClsPC: partially masked only through causality and the
 // sample bound (the diagonal block of a causal mask).  Both count as
@@ -88,26 +107,31 @@ enum Bar : int {
   kVEmpty = kVFull + kStages,      // [kStages]  PV MMAs done reading V
   kMFull = kVEmpty + kStages,      // [kMetaSlots] tile metadata written
   kMEmpty = kMFull + kMetaSlots,   // [kMetaSlots] metadata consumed
-  kQFull = kMEmpty + kMetaSlots,   // both Q tiles of the item landed
-  kQEmpty,                         // last S MMA of the item done
-  kSFull,                          // [2] S_i ready
-  kPFull = kSFull + 2,             // [2] P_i written (128 arrivals)
-  kOFull = kPFull + 2,             // [2] last PV_i of the item done
-  kOEmpty = kOFull + 2,            // [2] O_i read by the epilogue (128 arrivals)
-  kDrain = kOEmpty + 2,
-  kNumBars
+  kQFull = kMEmpty + kMetaSlots,   // [2 buffers] both Q tiles of an item landed
+  kQEmpty = kQFull + 2,            // [2 buffers] last S MMA of the item done
+  kSFull = kQEmpty + 2,            // [2 tiles][2 buffers] S_i ready
+  kPFull = kSFull + 4,             // [2 tiles][2 buffers] P_i written (128 arrivals)
+  kOFull = kPFull + 4,             // [2] last PV_i of the item done (one S buffer)
+  kPVDone = kOFull + 2,            // [2 tiles][2 buffers] PV_i done (two S buffers)
+  kOEmpty = kPVDone + 4,           // [2] O_i read by the epilogue (128 arrivals)
+  kSLoaded = kOEmpty + 2,          // [2] S_i is in registers (one S buffer; 128 arrivals)
+  kPHalf = kSLoaded + 2,           // [2] first half of P_i written (one S buffer; 128 arrivals)
+  kDrain = kPHalf + 2,             // [2] an issuer's MMAs are all done
+  kNumBars = kDrain + 2
 };
 
-// arrivals on kMEmpty: the V producer lane and the eight softmax warps
-constexpr int kMEmptyCount = 9;
+// arrivals on kMEmpty: the V producer lane, the MMA issuers and the eight
+// softmax warps
+template <int BN>
+constexpr int kMEmptyCount = 9 + kIssuers<BN>;
 
 template <int D, int BN>
 struct Layout {
   static constexpr int kQBytes = kTileM * D * 2;  // one Q tile
   static constexpr int kKBytes = BN * D * 2;
   static constexpr int kVBytes = BN * D * 2;
-  static constexpr int kQ = 0;  // 2 Q tiles
-  static constexpr int kK = kQ + 2 * kQBytes;
+  static constexpr int kQ = 0;  // kBufs buffers of 2 Q tiles
+  static constexpr int kK = kQ + kBufs<BN> * 2 * kQBytes;
   static constexpr int kV = kK + kStages * kKBytes;
   static constexpr int kCols = kV + kStages * kVBytes;  // int32 [kMetaSlots][4][BN]
   static constexpr int kMeta = kCols + kMetaSlots * 4 * BN * 4;
@@ -117,8 +141,8 @@ struct Layout {
   static constexpr int kEnd = kAbort + 4;
   static constexpr int kBytes = kEnd + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  // TMEM columns: S_i at i*128 (P_i packed into its first BN/2 columns),
-  // O_i at 256 + i*128.
+  // TMEM columns: S_i of buffer b at i*128 + b*BN (P_i packed into its first
+  // BN/2 columns), O_i at 256 + i*128.
   static_assert(BN <= 128 && D <= 128, "TMEM budget");
   static_assert(kBytes <= 232448, "shared memory budget");
 };
@@ -294,6 +318,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
       "r"(r[15])
+      : "memory");
+}
+
+// 16 consecutive 32-bit columns per lane, with the wait.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
       : "memory");
 }
 
@@ -541,6 +578,45 @@ __device__ __forceinline__ void umma_commit_elect(uint64_t* bar) {
       : "memory");
 }
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+
+__device__ __forceinline__ float sum_f32x2(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo + hi;
+}
+
+// Two softmax numerators at once: p_k = 2^(s_k * scale + base) with one
+// packed FMA and two ex2; (p0, p1) is added to the packed partial sums and
+// returned as bf16x2 (p0 in the low half).
+__device__ __forceinline__ uint32_t exp2_pair_bf16(uint32_t s0, uint32_t s1, uint64_t scale2,
+                                                   uint64_t base2, uint64_t& sum2) {
+  uint32_t packed;
+  asm("{\n\t.reg .b64 x, y, p;\n\t.reg .f32 y0, y1, p0, p1;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "fma.rn.f32x2 y, x, %4, %5;\n\t"
+      "mov.b64 {y0, y1}, y;\n\t"
+      "ex2.approx.ftz.f32 p0, y0;\n\t"
+      "ex2.approx.ftz.f32 p1, y1;\n\t"
+      "mov.b64 p, {p0, p1};\n\t"
+      "add.f32x2 %1, %1, p;\n\t"
+      "cvt.rn.bf16x2.f32 %0, p1, p0;\n\t}"
+      : "=r"(packed), "+l"(sum2)
+      : "r"(s0), "r"(s1), "l"(scale2), "l"(base2));
+  return packed;
+}
+
 struct Sync {
   uint64_t* bars;
   volatile int* abort;
@@ -557,8 +633,10 @@ struct Sync {
     fail();
     return false;
   }
-  // every lane waits; the warp proceeds only if all lanes saw the phase
+  // every lane waits; the warp proceeds only if all lanes saw the phase.
+  // A phase that has already completed costs one test and one vote.
   __device__ __forceinline__ bool warp(int bar, uint32_t parity) const {
+    if (__all_sync(0xffffffffu, mbar_test_wait(&bars[bar], parity))) return true;
     const bool ok = mbar_wait_bounded(&bars[bar], parity, tmo, abort);
     const bool all = __all_sync(0xffffffffu, ok);
     if (!all && lane == 0) fail();
@@ -589,23 +667,29 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&bars[kKFull + i], 1);
-      mbar_init(&bars[kKEmpty + i], 1);
+      mbar_init(&bars[kKEmpty + i], kIssuers<BN>);
       mbar_init(&bars[kVFull + i], 1);
-      mbar_init(&bars[kVEmpty + i], 1);
+      mbar_init(&bars[kVEmpty + i], kIssuers<BN>);
     }
     for (int i = 0; i < kMetaSlots; ++i) {
       mbar_init(&bars[kMFull + i], 1);
-      mbar_init(&bars[kMEmpty + i], kMEmptyCount);
+      mbar_init(&bars[kMEmpty + i], kMEmptyCount<BN>);
     }
-    mbar_init(&bars[kQFull], 1);
-    mbar_init(&bars[kQEmpty], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[kSFull + i], 1);
-      mbar_init(&bars[kPFull + i], 128);
+      mbar_init(&bars[kQFull + i], 1);
+      mbar_init(&bars[kQEmpty + i], kIssuers<BN>);
       mbar_init(&bars[kOFull + i], 1);
       mbar_init(&bars[kOEmpty + i], 128);
+      mbar_init(&bars[kSLoaded + i], 128);
+      mbar_init(&bars[kPHalf + i], 128);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&bars[kPVDone + i], 1);
+      mbar_init(&bars[kSFull + i], 1);
+      mbar_init(&bars[kPFull + i], 128);
     }
     mbar_init(&bars[kDrain], 1);
+    mbar_init(&bars[kDrain + 1], 1);
     *abort_flag = 0;
     mbar_fence_init();
     tma_prefetch_desc(&tq);
@@ -629,7 +713,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
     uint32_t mslot = 0, mround = 0;  // metadata ring
     uint32_t q_round = 0;
     uint32_t k_armed[kStages] = {0xffffffffu, 0xffffffffu};
-    uint32_t q_armed = 0xffffffffu;
+    uint32_t q_armed[2] = {0xffffffffu, 0xffffffffu};
     long long cnt_p = 0, cnt_u = 0, cnt_f = 0;
     bool ok = true;
 
@@ -769,25 +853,28 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
             break;
           }
           if (pushed == 0) {
-            // Q tiles of this item, once the previous item's S MMAs are done
-            if (!sy.warp(kQEmpty, (q_round & 1) ^ 1)) {
+            // Q tiles of this item into Q buffer q_round % kBufs, once the S
+            // MMAs of the item that used that buffer last are done
+            const uint32_t qb = q_round % kBufs<BN>;
+            if (!sy.warp(kQEmpty + qb, ((q_round / kBufs<BN>) & 1) ^ 1)) {
               ok = false;
               break;
             }
             if (lane == 0) {
-              mbar_arrive_expect_tx(&bars[kQFull], (has_q1 ? 2 : 1) * L::kQBytes);
+              uint8_t* qdst = smem + L::kQ + qb * 2 * L::kQBytes;
+              mbar_arrive_expect_tx(&bars[kQFull + qb], (has_q1 ? 2 : 1) * L::kQBytes);
 #pragma unroll
               for (int c = 0; c < D / 64; ++c)
-                tma_load_2d(smem + L::kQ + c * (kTileM * 128), &tq, &bars[kQFull],
+                tma_load_2d(qdst + c * (kTileM * 128), &tq, &bars[kQFull + qb],
                             h * D + c * 64, r0);
               if (has_q1) {
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
-                  tma_load_2d(smem + L::kQ + L::kQBytes + c * (kTileM * 128), &tq,
-                              &bars[kQFull], h * D + c * 64, r0 + BM);
+                  tma_load_2d(qdst + L::kQBytes + c * (kTileM * 128), &tq,
+                              &bars[kQFull + qb], h * D + c * 64, r0 + BM);
               }
             }
-            q_armed = q_round;
+            q_armed[qb] = q_round;
             ++q_round;
           }
           if (!sy.warp(kKEmpty + kst, (kround & 1) ^ 1)) {
@@ -815,8 +902,10 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       for (int st = 0; st < kStages; ++st)
         if (k_armed[st] != 0xffffffffu)
           mbar_wait_bounded(&bars[kKFull + st], k_armed[st] & 1, 100000000ull, nullptr);
-      if (q_armed != 0xffffffffu)
-        mbar_wait_bounded(&bars[kQFull], q_armed & 1, 100000000ull, nullptr);
+      for (int qb = 0; qb < 2; ++qb)
+        if (q_armed[qb] != 0xffffffffu)
+          mbar_wait_bounded(&bars[kQFull + qb], (q_armed[qb] / kBufs<BN>) & 1, 100000000ull,
+                            nullptr);
     }
     if (lane == 0 && p.class_counts != nullptr) {
       atomicAdd(reinterpret_cast<unsigned long long*>(p.class_counts + 0),
@@ -865,11 +954,14 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
     }
     attn_teardown<D, BN>(tmem_slot, warp);
     return;
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || (warp == 3 && kIssuers<BN> == 2)) {
+    // ----------------------------------------------------------------- MMA issuers
     // The whole warp runs this loop (every branch condition is warp-uniform);
-    // MMAs and commits are issued by the lane elect.sync picks.
+    // MMAs and commits are issued by the lane elect.sync picks.  Both issuers
+    // walk the same tile sequence (metadata, K and V rings); issuer `me`
+    // issues only for Q tile `me` when there are two.
     {
+      const int me = warp == 1 ? 0 : 1;
       constexpr uint32_t kIdescS = idesc_bf16_f32(kTileM, BN, false);
       constexpr uint32_t kIdescO = idesc_bf16_f32(kTileM, D, true);
       const uint32_t q_addr = smem_u32(smem + L::kQ);
@@ -885,6 +977,8 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       auto next_flags = [&](int& flags) -> bool {
         if (!sy.warp(kMFull + mslot, mround & 1)) return false;
         flags = *reinterpret_cast<volatile int*>(&meta[mslot].flags);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kMEmpty + mslot]);
         if (++mslot == kMetaSlots) {
           mslot = 0;
           ++mround;
@@ -897,10 +991,10 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       const uint64_t q_desc0 = sdesc_sw128(q_addr, 16, 1024);
       const uint64_t k_desc0 = sdesc_sw128(k_addr, 16, 1024);
       const uint64_t v_desc0 = sdesc_sw128(v_addr, BN * 128, 1024);
-      // S_i = Q_i K^T for the K tile in stage kst
-      auto issue_s = [&](int i) {
-        const uint32_t d_tmem = tmem_base + i * 128;
-        const uint64_t qd = q_desc0 + static_cast<uint64_t>(i * (L::kQBytes >> 4));
+      // S_i = Q_i K^T for the K tile in stage kst, Q buffer qb, into S buffer sb
+      auto issue_s = [&](int i, uint32_t sb, uint32_t qb) {
+        const uint32_t d_tmem = tmem_base + i * 128 + sb * BN;
+        const uint64_t qd = q_desc0 + static_cast<uint64_t>((qb * 2 + i) * (L::kQBytes >> 4));
         const uint64_t kd = k_desc0 + static_cast<uint64_t>(kst * (L::kKBytes >> 4));
         constexpr int QC = (kTileM * 128) >> 4;  // next 64-column chunk of Q
         constexpr int KC = (BN * 128) >> 4;      // next 64-column chunk of K
@@ -910,12 +1004,11 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         } else {
           umma_ss_group4<2, 2, 4, 4, 6, 6>(d_tmem, qd, kd, kIdescS, 0u);
         }
-        umma_commit_elect(&bars[kSFull + i]);
       };
-      // O_i (+)= P_i V for the V tile in stage vst
-      auto issue_pv = [&](int i, bool first) {
+      // O_i (+)= P_i V for the V tile in stage vst, P_i in S buffer sb
+      auto issue_pv = [&](int i, bool first, uint32_t sb) {
         const uint32_t d_tmem = tmem_base + 256 + i * 128;
-        const uint32_t a_tmem = tmem_base + i * 128;
+        const uint32_t a_tmem = tmem_base + i * 128 + sb * BN;
         const uint64_t vd = v_desc0 + static_cast<uint64_t>(vst * (L::kVBytes >> 4));
         constexpr int VS = (16 * 128) >> 4;  // 16 rows of V per K=16 step
         if constexpr (BN == 128) {
@@ -924,94 +1017,237 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
           umma_ts_group4<VS>(d_tmem, a_tmem, vd, kIdescO, first ? 0u : 1u);
         }
       };
-      // S MMAs of the first tile of an item (waits for its Q tiles and K)
-      auto start_item = [&](int flags) -> bool {
-        if (!sy.warp(kQFull, q_round & 1)) return false;
-        ++q_round;
-        if (!sy.warp(kKFull + kst, kround & 1)) return false;
-        tc_fence_after();
-        issue_s(0);
-        if (flags & kHasQ1) issue_s(1);
-        umma_commit_elect(&bars[kKEmpty + kst]);
-        if (flags & kLast) umma_commit_elect(&bars[kQEmpty]);
+      auto advance_k = [&]() {
         if (++kst == kStages) {
           kst = 0;
           ++kround;
         }
-        return true;
       };
-      auto wait_pv_ready = [&](int i, bool first) -> bool {
+      auto advance_v = [&]() {
+        if (++vst == kStages) {
+          vst = 0;
+          ++vround;
+        }
+      };
+      auto wait_o_empty = [&](int i, bool first) -> bool {
         if (first && o_pending[i]) {
           if (!sy.warp(kOEmpty + i, o_round[i] & 1)) return false;
           ++o_round[i];
           o_pending[i] = false;
         }
-        if (!sy.warp(kPFull + i, p_round[i] & 1)) return false;
-        ++p_round[i];
-        tc_fence_after();
         return true;
       };
 
-      int cur = 0;
-      ok = next_flags(cur);
-      if (ok && !(cur & kStop)) ok = start_item(cur);
-      while (ok && !(cur & kStop)) {
-        const bool first = (cur & kFirst) != 0;
-        const bool last = (cur & kLast) != 0;
-        const bool q1 = (cur & kHasQ1) != 0;
-        int nxt = 0;
-        if (!sy.warp(kVFull + vst, vround & 1)) { ok = false; break; }
-        // tile 0: PV, then S of the next KV tile (P_0 is read before S_0 is
-        // overwritten: MMAs from one thread run in issue order)
-        if (!wait_pv_ready(0, first)) { ok = false; break; }
-        issue_pv(0, first);
-        if (last) {
-          umma_commit_elect(&bars[kOFull + 0]);
-          o_pending[0] = true;
-        }
-        if (!last) {
-          if (!sy.warp(kKFull + kst, kround & 1)) { ok = false; break; }
+      if constexpr (kBufs<BN> == 2) {
+        // Two S buffers per Q tile.  The S stream runs two KV tiles ahead of
+        // the PV stream: for each tile t, PV_i(t) is followed by S_i(t+2),
+        // which overwrites the buffer PV_i(t) has just read (MMAs from one
+        // thread run in issue order), so the softmax of tile t+1 never waits
+        // for the MMAs of tile t.  Every buffer has its own S-full and P-full
+        // barrier: a warpgroup may finish P(t+1) before P(t) is waited for.
+        uint32_t q_seq = 0, qb = 0;             // items the S stream entered; its Q buffer
+        uint32_t s_cnt[2] = {0u, 0u};           // S_i issued (buffer = s_cnt & 1)
+        uint32_t pv_cnt[2] = {0u, 0u};          // PV_i issued (buffer = pv_cnt & 1)
+        uint32_t fq = 0u;  // 4-bit flags of the (at most four) tiles with S issued, PV not yet
+        uint32_t n_s = 0, n_pv = 0;
+        bool s_end = false;
+        // next tile of the S stream: its metadata, its item's Q buffer (first
+        // tile of an item) and its K tile
+        auto s_fetch = [&](int& flags) -> bool {
+          if (!next_flags(flags)) return false;
+          if (flags & kStop) {
+            s_end = true;
+            return true;
+          }
+          if (flags & kFirst) {
+            qb = q_seq & 1u;
+            if (!sy.warp(kQFull + qb, (q_seq >> 1) & 1u)) return false;
+            ++q_seq;
+          }
+          if (!sy.warp(kKFull + kst, kround & 1)) return false;
           tc_fence_after();
-          // the metadata of this K tile was written before its load was armed
-          nxt = *reinterpret_cast<volatile int*>(&meta[mslot].flags);
-          if (++mslot == kMetaSlots) {
-            mslot = 0;
-            ++mround;
-          }
-          issue_s(0);
-        }
-        // tile 1
-        if (q1) {
-          if (!wait_pv_ready(1, first)) { ok = false; break; }
-          issue_pv(1, first);
-          if (last) {
-            umma_commit_elect(&bars[kOFull + 1]);
-            o_pending[1] = true;
-          }
-          if (!last) issue_s(1);
-        }
-        umma_commit_elect(&bars[kVEmpty + vst]);
-        if (++vst == kStages) {
-          vst = 0;
-          ++vround;
-        }
-        if (!last) {
+          return true;
+        };
+        auto s_one = [&](int i) {
+          const uint32_t sb = s_cnt[i] & 1u;
+          issue_s(i, sb, qb);
+          umma_commit_elect(&bars[kSFull + 2 * i + sb]);
+          ++s_cnt[i];
+        };
+        auto s_done = [&](int flags) {
           umma_commit_elect(&bars[kKEmpty + kst]);
-          if (nxt & kLast) umma_commit_elect(&bars[kQEmpty]);
-          if (++kst == kStages) {
-            kst = 0;
-            ++kround;
+          if (flags & kLast) umma_commit_elect(&bars[kQEmpty + qb]);
+          advance_k();
+          const uint32_t sh = (n_s & 3u) * 4u;
+          fq = (fq & ~(0xFu << sh)) | (static_cast<uint32_t>(flags & 0xF) << sh);
+          ++n_s;
+        };
+        for (int w = 0; w < 2 && ok && !s_end; ++w) {
+          int f = 0;
+          if (!s_fetch(f)) {
+            ok = false;
+            break;
           }
-        } else {
-          if (!next_flags(nxt)) { ok = false; break; }
-          if (nxt & kStop) break;
-          if (!start_item(nxt)) { ok = false; break; }
+          if (s_end) break;
+          s_one(0);
+          if (f & kHasQ1) s_one(1);
+          s_done(f);
         }
-        cur = nxt;
+        while (ok && n_pv < n_s) {
+          const int cur = static_cast<int>((fq >> ((n_pv & 3u) * 4u)) & 0xFu);
+          const bool first = (cur & kFirst) != 0;
+          const bool last = (cur & kLast) != 0;
+          int nxt = 0;
+          bool ahead = false;
+          if (!s_end) {
+            if (!s_fetch(nxt)) { ok = false; break; }
+            ahead = !s_end;
+          }
+          if (!sy.warp(kVFull + vst, vround & 1)) { ok = false; break; }
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            if (i == 0 || (cur & kHasQ1)) {
+              const uint32_t sb = pv_cnt[i] & 1u;
+              if (!wait_o_empty(i, first)) { ok = false; break; }
+              if (!sy.warp(kPFull + 2 * i + sb, (pv_cnt[i] >> 1) & 1u)) { ok = false; break; }
+              tc_fence_after();
+              issue_pv(i, first, sb);
+              umma_commit_elect(&bars[kPVDone + 2 * i + sb]);
+              ++pv_cnt[i];
+              if (last) o_pending[i] = true;
+            }
+            if (ahead && (i == 0 || (nxt & kHasQ1))) s_one(i);
+          }
+          if (!ok) break;
+          umma_commit_elect(&bars[kVEmpty + vst]);
+          advance_v();
+          if (ahead) s_done(nxt);
+          ++n_pv;
+        }
+      } else {
+        // One S buffer per Q tile, one issuer per Q tile (i = me).  Per KV
+        // tile: the upper half of S_i(next) as soon as the softmax holds S_i
+        // in registers, PV_i in two halves as the two halves of P_i land,
+        // then the lower half of S_i(next), which overwrites the columns P_i
+        // occupies (MMAs from one thread run in issue order).  Between the
+        // end of a softmax and its next S only the second PV half and the
+        // lower S half remain.  K, V and Q stages are released when both
+        // issuers have committed (their empty barriers count two arrivals).
+        constexpr uint32_t kIdescS64 = idesc_bf16_f32(kTileM, 64, false);
+        uint32_t sl_round[2] = {0u, 0u}, ph_round[2] = {0u, 0u};
+        // S MMAs (all BN key columns) of the first tile of an item
+        auto start_item = [&](int flags) -> bool {
+          if (!sy.warp(kQFull, q_round & 1)) return false;
+          ++q_round;
+          if (!sy.warp(kKFull + kst, kround & 1)) return false;
+          tc_fence_after();
+          if (me == 0 || (flags & kHasQ1)) {
+            issue_s(me, 0u, 0u);
+            umma_commit_elect(&bars[kSFull + 2 * me]);
+          }
+          umma_commit_elect(&bars[kKEmpty + kst]);
+          if (flags & kLast) umma_commit_elect(&bars[kQEmpty]);
+          advance_k();
+          return true;
+        };
+        // keys [64h, 64h + 64) of S_i = Q_i K^T for the K tile in stage kst
+        auto issue_s_half = [&](int i, int h) {
+          const uint32_t d_tmem = tmem_base + i * 128 + h * 64;
+          const uint64_t qd = q_desc0 + static_cast<uint64_t>(i * (L::kQBytes >> 4));
+          const uint64_t kd = k_desc0 + static_cast<uint64_t>(kst * (L::kKBytes >> 4)) +
+                              static_cast<uint64_t>(h * ((64 * 128) >> 4));
+          constexpr int QC = (kTileM * 128) >> 4;  // next 64-column chunk of Q
+          constexpr int KC = (BN * 128) >> 4;      // next 64-column chunk of K
+          if constexpr (D == 128) {
+            umma_ss_group8<2, 2, 4, 4, 6, 6, QC, KC, QC + 2, KC + 2, QC + 4, KC + 4, QC + 6, KC + 6>(
+                d_tmem, qd, kd, kIdescS64, 0u);
+          } else {
+            umma_ss_group4<2, 2, 4, 4, 6, 6>(d_tmem, qd, kd, kIdescS64, 0u);
+          }
+        };
+        // keys [64h, 64h + 64) of O_i (+)= P_i V for the V tile in stage vst
+        auto issue_pv_half = [&](int i, int h, uint32_t acc0) {
+          const uint32_t d_tmem = tmem_base + 256 + i * 128;
+          const uint32_t a_tmem = tmem_base + i * 128 + h * 32;
+          const uint64_t vd = v_desc0 + static_cast<uint64_t>(vst * (L::kVBytes >> 4)) +
+                              static_cast<uint64_t>(h * ((64 * 128) >> 4));
+          constexpr int VS = (16 * 128) >> 4;  // 16 rows of V per K=16 step
+          umma_ts_group4<VS>(d_tmem, a_tmem, vd, kIdescO, acc0);
+        };
+
+        int cur = 0;
+        ok = next_flags(cur);
+        if (ok && !(cur & kStop)) ok = start_item(cur);
+        while (ok && !(cur & kStop)) {
+          const bool first = (cur & kFirst) != 0;
+          const bool last = (cur & kLast) != 0;
+          const bool q1 = (cur & kHasQ1) != 0;
+          int nxt = 0;
+          if (!sy.warp(kVFull + vst, vround & 1)) { ok = false; break; }
+          if (!last) {
+            if (!sy.warp(kKFull + kst, kround & 1)) { ok = false; break; }
+            tc_fence_after();
+            // the metadata of this K tile was written before its load was armed
+            nxt = *reinterpret_cast<volatile int*>(&meta[mslot].flags);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kMEmpty + mslot]);
+            if (++mslot == kMetaSlots) {
+              mslot = 0;
+              ++mround;
+            }
+          }
+          if (me == 0 || q1) {
+            const int i = me;
+            if constexpr (kSplitHandoff) {
+              if (!sy.warp(kSLoaded + i, sl_round[i] & 1)) { ok = false; break; }
+              ++sl_round[i];
+              tc_fence_after();
+              if (!last) issue_s_half(i, 1);
+            }
+            if (!wait_o_empty(i, first)) { ok = false; break; }
+            if constexpr (kSplitHandoff) {
+              if (!sy.warp(kPHalf + i, ph_round[i] & 1)) { ok = false; break; }
+              ++ph_round[i];
+              tc_fence_after();
+              issue_pv_half(i, 0, first ? 0u : 1u);
+            }
+            if (!sy.warp(kPFull + 2 * i, p_round[i] & 1)) { ok = false; break; }
+            ++p_round[i];
+            tc_fence_after();
+            if constexpr (kSplitHandoff) {
+              issue_pv_half(i, 1, 1u);
+            } else {
+              issue_pv(i, first, 0u);
+            }
+            if (last) {
+              umma_commit_elect(&bars[kOFull + i]);
+              o_pending[i] = true;
+            } else {
+              if constexpr (kSplitHandoff) {
+                issue_s_half(i, 0);
+              } else {
+                issue_s(i, 0u, 0u);
+              }
+              umma_commit_elect(&bars[kSFull + 2 * i]);
+            }
+          }
+          umma_commit_elect(&bars[kVEmpty + vst]);
+          advance_v();
+          if (!last) {
+            umma_commit_elect(&bars[kKEmpty + kst]);
+            if (nxt & kLast) umma_commit_elect(&bars[kQEmpty]);
+            advance_k();
+          } else {
+            if (!next_flags(nxt)) { ok = false; break; }
+            if (nxt & kStop) break;
+            if (!start_item(nxt)) { ok = false; break; }
+          }
+          cur = nxt;
+        }
       }
       // all issued MMAs complete before TMEM is released
-      umma_commit_elect(&bars[kDrain]);
-      mbar_wait_bounded(&bars[kDrain], 0, 100000000ull, nullptr);
+      umma_commit_elect(&bars[kDrain + me]);
+      mbar_wait_bounded(&bars[kDrain + me], 0, 100000000ull, nullptr);
     }
     attn_teardown<D, BN>(tmem_slot, warp);
     return;
@@ -1052,7 +1288,7 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
     const float scale_log2 = p.scale_log2;
     const bool causal = p.causal != 0;
     uint32_t mslot = 0, mround = 0;
-    uint32_t s_round = 0, o_round = 0;
+    uint32_t n_tiles = 0, o_round = 0;  // KV tiles of this warpgroup so far; epilogues
     float m_run = -CUDART_INF_F, l_run = 0.f;
     int rt0 = 0, rt1 = 0, h = 0;
 
@@ -1087,10 +1323,6 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
         m_run = -CUDART_INF_F;
         l_run = 0.f;
       }
-      if (!sy.warp(kSFull + wg, s_round & 1)) break;
-      ++s_round;
-      tc_fence_after();
-
       const int r = rt0 + row;
       const int valid = c1 - c0;  // columns inside the sample
       uint32_t mbits[BN / 32];    // element mask of a partially masked block
@@ -1140,39 +1372,55 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kMEmpty + cur_slot]);
 
+      // S buffer of this tile and the parity of its S-full / P-full phase
+      const uint32_t sb = n_tiles % kBufs<BN>;
+      const uint32_t spar = (n_tiles / kBufs<BN>) & 1u;
+      const uint32_t s_cur = s_tmem + sb * BN;
+      if (!sy.warp(kSFull + 2 * wg + sb, spar)) break;
+      tc_fence_after();
+
+      bool o_ok = true;
       if (cls == kClsF) {
         // live only for the other Q tile: contributes nothing, P = 0
+        if constexpr (kBufs<BN> == 1 && kSplitHandoff) {
+          tc_fence_before();
+          mbar_arrive(&bars[kSLoaded + wg]);
+        }
         uint32_t z[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) z[i] = 0u;
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) tmem_st16(s_tmem + c * 16, z);
+        for (int c = 0; c < BN / 32; ++c) tmem_st16(s_cur + c * 16, z);
         tmem_st_wait();
+        if constexpr (kBufs<BN> == 1 && kSplitHandoff) {
+          tc_fence_before();
+          mbar_arrive(&bars[kPHalf + wg]);
+        }
       } else {
         // the whole S row in registers: one TMEM load, one wait
         uint32_t sr[BN];
-        tmem_ld_row<BN>(s_tmem, sr);
-        float m8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = -CUDART_INF_F;
+        tmem_ld_row<BN>(s_cur, sr);
+        if constexpr (kBufs<BN> == 1 && kSplitHandoff) {
+          // S is in registers: the MMAs of the next KV tile may overwrite the
+          // upper half of these columns (P only ever occupies the lower half)
+          tc_fence_before();
+          mbar_arrive(&bars[kSLoaded + wg]);
+        }
         if (cls == kClsP || cls == kClsPC) {
 #pragma unroll
-          for (int j = 0; j < BN; ++j) {
+          for (int j = 0; j < BN; ++j)
             if ((mbits[j >> 5] >> (j & 31)) & 1u) sr[j] = __float_as_uint(-CUDART_INF_F);
-            m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j]));
-          }
         } else if (valid < BN) {
 #pragma unroll
-          for (int j = 0; j < BN; ++j) {
+          for (int j = 0; j < BN; ++j)
             if (j >= valid) sr[j] = __float_as_uint(-CUDART_INF_F);
-            m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j]));
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < BN; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j]));
         }
-        const float mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        // row max, two new elements per three-input max
+        float m4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+#pragma unroll
+        for (int j = 0; j < BN; j += 2)
+          m4[(j >> 1) & 3] = fmax3(m4[(j >> 1) & 3], __uint_as_float(sr[j]), __uint_as_float(sr[j + 1]));
+        const float mt = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
         // scores in the log2 domain: x = s * scale * log2(e)
         const float mt2 = mt * scale_log2;
         const float m_new = fmaxf(m_run, mt2);
@@ -1188,10 +1436,36 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
         if (resc) l_run = first ? 0.f : l_run * factor;
         m_run = m_ref;
 
-        const float neg_base = (m_ref == -CUDART_INF_F) ? 0.f : -m_ref;
-        float sum8[8];
+        if (__any_sync(0xffffffffu, need_o)) {
+          // rescale O before any part of this tile's P reaches a PV MMA.
+          // One S buffer: the previous PV completed before S (the lower half
+          // of S was issued after it).  Two S buffers: S was issued before
+          // the previous PV, so wait for that PV here.  Its done barrier belongs
+          // to its S buffer; the barrier's previous phase (the PV two tiles
+          // back) completed before this tile's S, so the parity is exact.
+          if constexpr (kBufs<BN> == 2) {
+            const uint32_t pt = n_tiles - 1u;
+            o_ok = sy.warp(kPVDone + 2 * wg + (pt & 1u), (pt >> 1) & 1u);
+            tc_fence_after();
+          }
+          if (o_ok) {
+            const float f = need_o ? factor : 1.f;
+            // 16 columns at a time: the S row is still live in registers
+#pragma unroll 1
+            for (int c = 0; c < D / 16; ++c) {
+              uint32_t rr[16];
+              tmem_ld16(o_tmem + c * 16, rr);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sum8[i] = 0.f;
+              for (int i = 0; i < 16; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * f);
+              tmem_st16(o_tmem + c * 16, rr);
+            }
+            tmem_st_wait();
+          }
+        }
+        const float neg_base = (m_ref == -CUDART_INF_F) ? 0.f : -m_ref;
+        const uint64_t scale2 = pack_f32x2(scale_log2, scale_log2);
+        const uint64_t base2 = pack_f32x2(neg_base, neg_base);
+        uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};  // eight partial row sums
         // P = 2^(x - m) as bf16 into the first half of the S columns
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
@@ -1199,36 +1473,33 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
             const int j = c * 32 + i;
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[j]), scale_log2, neg_base));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[j + 1]), scale_log2, neg_base));
-            sum8[(i >> 1) & 7] += p0 + p1;
-            pk[i >> 1] = pack_bf16x2(p0, p1);
+            pk[i >> 1] = exp2_pair_bf16(sr[j], sr[j + 1], scale2, base2, sum2[(i >> 1) & 3]);
           }
-          tmem_st16(s_tmem + c * 16, pk);
+          tmem_st16(s_cur + c * 16, pk);
+          if constexpr (kBufs<BN> == 1 && kSplitHandoff) {
+            if (c == BN / 64 - 1) {
+              // the first half of P is in TMEM: its PV MMAs may start
+              tmem_st_wait();
+              tc_fence_before();
+              mbar_arrive(&bars[kPHalf + wg]);
+            }
+          }
         }
         tmem_st_wait();
-        l_run += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                 ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-        if (__any_sync(0xffffffffu, need_o)) {
-          // rescale O before the PV of this tile is issued (it waits for P);
-          // the previous PV completed before S, which was committed after it
-          const float f = need_o ? factor : 1.f;
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t rr[32];
-            tmem_ld32(o_tmem + c * 32, rr);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * f);
-            tmem_st32(o_tmem + c * 32, rr);
-          }
-          tmem_st_wait();
-        }
+        l_run += (sum_f32x2(sum2[0]) + sum_f32x2(sum2[1])) + (sum_f32x2(sum2[2]) + sum_f32x2(sum2[3]));
       }
+      if (!o_ok) break;
       tc_fence_before();
-      mbar_arrive(&bars[kPFull + wg]);
+      mbar_arrive(&bars[kPFull + 2 * wg + sb]);
 
       if (flags & kLast) {
-        if (!sy.warp(kOFull + wg, o_round & 1)) break;
+        // O_i is final once the PV of this tile is done (MMAs complete in
+        // issue order, so every earlier PV is done too)
+        if constexpr (kBufs<BN> == 2) {
+          if (!sy.warp(kPVDone + 2 * wg + sb, spar)) break;
+        } else {
+          if (!sy.warp(kOFull + wg, o_round & 1)) break;
+        }
         ++o_round;
         tc_fence_after();
         const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
@@ -1261,6 +1532,7 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
         tc_fence_before();
         mbar_arrive(&bars[kOEmpty + wg]);
       }
+      ++n_tiles;
     }
     attn_teardown<D, BN>(tmem_slot, warp);
   }

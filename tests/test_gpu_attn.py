@@ -121,15 +121,39 @@ def test_small_mask_shapes(fm, head_dim, blocks, mask, causal):
 @pytest.mark.parametrize("seed", range(3))
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("per_head", [False, True])
-def test_random_intervals(fm, seed, causal, per_head):
+@pytest.mark.parametrize("block_n", [128, 64])
+def test_random_intervals(fm, seed, causal, per_head, block_n):
     """Arbitrary column intervals: many partial blocks, fully masked rows."""
     wl = gen.make_custom([3, 200, 129, 0, 64, 400], n_heads_q=4, n_heads_kv=1, head_dim=128,
                          mask="random", causal=causal, seed=seed,
                          n_mask_heads=4 if per_head else 1)
-    out, lse, counts, _ = run_attn(fm, wl)
+    out, lse, counts, _ = run_attn(fm, wl, block_n=block_n)
     ref = oracle(wl)
     compare(out, lse, ref, what="random")
-    assert counts == expected_counts(wl, 128, 128)
+    assert counts == expected_counts(wl, 128, block_n)
+
+
+@pytest.mark.parametrize("blocks", [(128, 128), (128, 64), (64, 64)])
+def test_growing_scores_rescale_o(fm, blocks):
+    """A score bias that grows along every sample (q[..., 0] = 1, k[..., 0] =
+    0.3 * position) raises the running row max by more than 2^8 every few
+    KV tiles, so O is rescaled in TMEM many times within an item (with two S
+    buffers: after waiting for the previous PV).  The bias is gentle enough
+    that each row still spreads its weight over tens of keys."""
+    import dataclasses
+    lens = [700, 300, 1500]
+    wl = gen.make_custom(lens, n_heads_q=4, n_heads_kv=2, head_dim=128,
+                         mask="causal_document", seed=11)
+    q = gen.bf16_bits_to_f32(wl.q_bits)
+    k = gen.bf16_bits_to_f32(wl.k_bits)
+    pos = np.concatenate([np.arange(n) for n in lens]).astype(np.float32)
+    q[:, :, 0] = 1.0
+    k[:, :, 0] = 0.3 * pos[:, None]
+    wl = dataclasses.replace(wl, q_bits=gen.f32_to_bf16_bits(q), k_bits=gen.f32_to_bf16_bits(k))
+    bm, bn = blocks
+    out, lse, counts, _ = run_attn(fm, wl, block_m=bm, block_n=bn)
+    compare(out, lse, oracle(wl), what=f"growing scores {bm}x{bn}")
+    assert counts == expected_counts(wl, bm, bn)
 
 
 def test_every_row_masked(fm):
@@ -186,20 +210,22 @@ def _sample_rows(wl, block_m, rng, extra=2000):
 
 
 @pytest.mark.parametrize("cfg", [2, 3, 4])
-def test_full_size_configs_sampled(fm, cfg):
+@pytest.mark.parametrize("block_n", [128, 64])
+def test_full_size_configs_sampled(fm, cfg, block_n):
     wl = gen.make_workload(cfg, seed=0)
-    out, lse, counts, _ = run_attn(fm, wl)
+    out, lse, counts, _ = run_attn(fm, wl, block_n=block_n)
     rng = np.random.default_rng(cfg)
     rows = _sample_rows(wl, 128, rng)
     heads = sorted(set([0, wl.n_heads_q - 1] + list(rng.integers(0, wl.n_heads_q, 2))))
     ref = oracle(wl, rows=rows, heads=heads)
     compare(out, lse, ref, rows=rows, heads=heads, what=f"cfg{cfg}")
-    assert counts == expected_counts(wl, 128, 128)
+    assert counts == expected_counts(wl, 128, block_n)
 
 
-def test_long_context_sampled(fm):
+@pytest.mark.parametrize("block_n", [128, 64])
+def test_long_context_sampled(fm, block_n):
     wl = gen.make_workload(5, seed=0)
-    out, lse, counts, _ = run_attn(fm, wl)
+    out, lse, counts, _ = run_attn(fm, wl, block_n=block_n)
     rng = np.random.default_rng(5)
     rows = _sample_rows(wl, 128, rng, extra=300)
     rows = np.unique(np.concatenate([rows, np.arange(65536 - 256, 65536),
@@ -207,7 +233,7 @@ def test_long_context_sampled(fm):
     heads = [0, 13, 31]
     ref = oracle(wl, rows=rows, heads=heads)
     compare(out, lse, ref, rows=rows, heads=heads, what="cfg5")
-    assert counts == expected_counts(wl, 128, 128)
+    assert counts == expected_counts(wl, 128, block_n)
 
 
 def test_int64_path_bit_identical(fm):
