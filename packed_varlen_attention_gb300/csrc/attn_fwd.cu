@@ -72,11 +72,10 @@ constexpr int kPrefetchAhead = 3;  // K/V tiles pulled into L2 ahead of their lo
 template <int BN>
 constexpr int kBufs = (BN == 64) ? 2 : 1;
 
-// MMA issuing warps.  With one S buffer each Q tile has its own issuer (warps
-// 1 and 3), so one tile's barrier waits never hold up the other tile's MMAs;
-// with two S buffers warp 1 issues for both.
+// MMA issuing warps: each Q tile has its own issuer (warps 1 and 3), so one
+// tile's barrier waits never hold up the other tile's MMAs.
 template <int BN>
-constexpr int kIssuers = (BN == 64) ? 1 : 2;
+constexpr int kIssuers = 2;
 
 // One S buffer: hand S and P over in 64-column halves (the upper half of the
 // next S starts once the softmax holds S in registers, PV starts on the first
@@ -954,7 +953,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
     }
     attn_teardown<D, BN>(tmem_slot, warp);
     return;
-  } else if (warp == 1 || (warp == 3 && kIssuers<BN> == 2)) {
+  } else if (warp == 1 || warp == 3) {
     // ----------------------------------------------------------------- MMA issuers
     // The whole warp runs this loop (every branch condition is warp-uniform);
     // MMAs and commits are issued by the lane elect.sync picks.  Both issuers
@@ -1039,8 +1038,9 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       };
 
       if constexpr (kBufs<BN> == 2) {
-        // Two S buffers per Q tile.  The S stream runs two KV tiles ahead of
-        // the PV stream: for each tile t, PV_i(t) is followed by S_i(t+2),
+        // Two S buffers per Q tile (i = me: this issuer's tile).  The S
+        // stream runs two KV tiles ahead of the PV stream: for each tile t,
+        // PV_i(t) is followed by S_i(t+2),
         // which overwrites the buffer PV_i(t) has just read (MMAs from one
         // thread run in issue order), so the softmax of tile t+1 never waits
         // for the MMAs of tile t.  Every buffer has its own S-full and P-full
@@ -1089,8 +1089,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
             break;
           }
           if (s_end) break;
-          s_one(0);
-          if (f & kHasQ1) s_one(1);
+          if (me == 0 || (f & kHasQ1)) s_one(me);
           s_done(f);
         }
         while (ok && n_pv < n_s) {
@@ -1104,8 +1103,8 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
             ahead = !s_end;
           }
           if (!sy.warp(kVFull + vst, vround & 1)) { ok = false; break; }
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
+          {
+            const int i = me;
             if (i == 0 || (cur & kHasQ1)) {
               const uint32_t sb = pv_cnt[i] & 1u;
               if (!wait_o_empty(i, first)) { ok = false; break; }
@@ -1118,7 +1117,6 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
             }
             if (ahead && (i == 0 || (nxt & kHasQ1))) s_one(i);
           }
-          if (!ok) break;
           umma_commit_elect(&bars[kVEmpty + vst]);
           advance_v();
           if (ahead) s_done(nxt);
@@ -1294,20 +1292,20 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
 
     for (;;) {
       if (!sy.warp(kMFull + mslot, mround & 1)) break;
-      const TileMeta* mp = meta + mslot;
-      const int flags = *reinterpret_cast<const volatile int*>(&mp->flags);
+      // the slot's first 32 bytes, {flags, cls0, cls1, c0} and {c1, r0,
+      // r_end, h}, in two loads (ordered after the acquiring wait above)
+      const int4 ma = *reinterpret_cast<const int4*>(meta + mslot);
+      const int4 mb = *(reinterpret_cast<const int4*>(meta + mslot) + 1);
+      const int flags = ma.x;
       if (flags & kStop) break;
-      const int cls = wg == 0 ? *reinterpret_cast<const volatile int*>(&mp->cls0)
-                              : *reinterpret_cast<const volatile int*>(&mp->cls1);
-      const int c0 = *reinterpret_cast<const volatile int*>(&mp->c0);
-      const int c1 = *reinterpret_cast<const volatile int*>(&mp->c1);
+      const int cls = wg == 0 ? ma.y : ma.z;
+      const int c0 = ma.w;
+      const int c1 = mb.x;
       const bool first = (flags & kFirst) != 0;
       if (first) {
-        const int r0 = *reinterpret_cast<const volatile int*>(&mp->r0);
-        const int r_end = *reinterpret_cast<const volatile int*>(&mp->r_end);
-        h = *reinterpret_cast<const volatile int*>(&mp->h);
-        rt0 = r0 + wg * BM;
-        rt1 = min(rt0 + BM, r_end);
+        h = mb.w;
+        rt0 = mb.y + wg * BM;
+        rt1 = min(rt0 + BM, mb.z);
       }
       const uint32_t cur_slot = mslot;
       if (++mslot == kMetaSlots) {
