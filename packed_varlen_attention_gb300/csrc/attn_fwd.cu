@@ -77,10 +77,13 @@ constexpr int kBufs = (BN == 64) ? 2 : 1;
 template <int BN>
 constexpr int kIssuers = 2;
 
-// One S buffer: hand S and P over in 64-column halves (the upper half of the
-// next S starts once the softmax holds S in registers, PV starts on the first
-// half of P) instead of whole tiles.
-constexpr bool kSplitHandoff = false;
+// One S buffer: the two issuers issue their blocks (PV_i of a tile and the
+// next S_i) strictly in turn, Q tile 0 first, so the tensor pipe runs one
+// tile's block after the other instead of interleaving them.
+constexpr bool kIssueTurns = true;
+
+// independent partial maxima per S row
+constexpr int kMaxChains = 4;
 
 // kClsP: partially masked through the column intervals (element mask from the
 // four vectors); kClsPC: partially masked only through causality and the
@@ -113,10 +116,9 @@ enum Bar : int {
   kOFull = kPFull + 4,             // [2] last PV_i of the item done (one S buffer)
   kPVDone = kOFull + 2,            // [2 tiles][2 buffers] PV_i done (two S buffers)
   kOEmpty = kPVDone + 4,           // [2] O_i read by the epilogue (128 arrivals)
-  kSLoaded = kOEmpty + 2,          // [2] S_i is in registers (one S buffer; 128 arrivals)
-  kPHalf = kSLoaded + 2,           // [2] first half of P_i written (one S buffer; 128 arrivals)
-  kDrain = kPHalf + 2,             // [2] an issuer's MMAs are all done
-  kNumBars = kDrain + 2
+  kDrain = kOEmpty + 2,            // [2] an issuer's MMAs are all done
+  kTurn = kDrain + 2,              // [2] issuer i may issue its next block
+  kNumBars = kTurn + 2
 };
 
 // arrivals on kMEmpty: the V producer lane, the MMA issuers and the eight
@@ -298,18 +300,6 @@ __global__ void __launch_bounds__(kCostBins) plan_order_kernel(const AttnParams 
 // TMEM helpers local to this kernel
 // ---------------------------------------------------------------------------
 
-// D[tmem] (+)= A[tmem] * B[smem]^T (A = P, bf16 packed two per column, the
-// even element in the low half).
-__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                 uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -363,6 +353,32 @@ __device__ __forceinline__ void tmem_ld_row<64>(uint32_t taddr, uint32_t (&r)[64
 template <>
 __device__ __forceinline__ void tmem_ld_row<128>(uint32_t taddr, uint32_t (&r)[128]) {
   tmem_ld128(taddr, r);
+}
+
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Masks columns [J0, J1) of an S row (mode 1: element bits, mode 2: columns
+// from `valid` on) and folds them into C independent partial maxima.
+template <int J0, int J1, int BN, int C>
+__device__ __forceinline__ void mask_and_max(uint32_t (&sr)[BN], const uint32_t (&mbits)[BN / 32],
+                                             int mode, int valid, float (&mc)[C]) {
+  if (mode == 1) {
+#pragma unroll
+    for (int j = J0; j < J1; ++j)
+      if ((mbits[j >> 5] >> (j & 31)) & 1u) sr[j] = __float_as_uint(-CUDART_INF_F);
+  } else if (mode == 2) {
+#pragma unroll
+    for (int j = J0; j < J1; ++j)
+      if (j >= valid) sr[j] = __float_as_uint(-CUDART_INF_F);
+  }
+#pragma unroll
+  for (int j = J0; j < J1; j += 2)
+    mc[(j >> 1) % C] = fmax3(mc[(j >> 1) % C], __uint_as_float(sr[j]), __uint_as_float(sr[j + 1]));
 }
 
 // Groups of MMAs issued from one asm block by the converged warp: every lane
@@ -577,12 +593,6 @@ __device__ __forceinline__ void umma_commit_elect(uint64_t* bar) {
       : "memory");
 }
 
-// max(a, b, c) in one instruction
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
 
 __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
   uint64_t d;
@@ -679,8 +689,6 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       mbar_init(&bars[kQEmpty + i], kIssuers<BN>);
       mbar_init(&bars[kOFull + i], 1);
       mbar_init(&bars[kOEmpty + i], 128);
-      mbar_init(&bars[kSLoaded + i], 128);
-      mbar_init(&bars[kPHalf + i], 128);
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bars[kPVDone + i], 1);
@@ -689,6 +697,8 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
     }
     mbar_init(&bars[kDrain], 1);
     mbar_init(&bars[kDrain + 1], 1);
+    mbar_init(&bars[kTurn], 1);
+    mbar_init(&bars[kTurn + 1], 1);
     *abort_flag = 0;
     mbar_fence_init();
     tma_prefetch_desc(&tq);
@@ -1124,55 +1134,44 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         }
       } else {
         // One S buffer per Q tile, one issuer per Q tile (i = me).  Per KV
-        // tile: the upper half of S_i(next) as soon as the softmax holds S_i
-        // in registers, PV_i in two halves as the two halves of P_i land,
-        // then the lower half of S_i(next), which overwrites the columns P_i
-        // occupies (MMAs from one thread run in issue order).  Between the
-        // end of a softmax and its next S only the second PV half and the
-        // lower S half remain.  K, V and Q stages are released when both
-        // issuers have committed (their empty barriers count two arrivals).
-        constexpr uint32_t kIdescS64 = idesc_bf16_f32(kTileM, 64, false);
-        uint32_t sl_round[2] = {0u, 0u}, ph_round[2] = {0u, 0u};
+        // tile: once P_i is in TMEM, PV_i and then S_i(next), which
+        // overwrites the columns P_i occupies (MMAs from one thread run in
+        // issue order).  K, V and Q stages are released when both issuers
+        // have committed (their empty barriers count two arrivals).
+        uint32_t turn_round = 0;
+        // strict alternation of the issuers' blocks (issuer 0 goes first: its
+        // first wait is on the phase before the barrier's first)
+        auto take_turn = [&]() -> bool {
+          if constexpr (kIssueTurns) {
+            const uint32_t par = (me == 0) ? ((turn_round & 1u) ^ 1u) : (turn_round & 1u);
+            if (!sy.warp(kTurn + me, par)) return false;
+            ++turn_round;
+          }
+          return true;
+        };
+        auto pass_turn = [&]() {
+          if constexpr (kIssueTurns) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kTurn + (me ^ 1)]);
+          }
+        };
         // S MMAs (all BN key columns) of the first tile of an item
         auto start_item = [&](int flags) -> bool {
           if (!sy.warp(kQFull, q_round & 1)) return false;
           ++q_round;
           if (!sy.warp(kKFull + kst, kround & 1)) return false;
           tc_fence_after();
+          if (!take_turn()) return false;
           if (me == 0 || (flags & kHasQ1)) {
             issue_s(me, 0u, 0u);
             umma_commit_elect(&bars[kSFull + 2 * me]);
           }
+          pass_turn();
           umma_commit_elect(&bars[kKEmpty + kst]);
           if (flags & kLast) umma_commit_elect(&bars[kQEmpty]);
           advance_k();
           return true;
         };
-        // keys [64h, 64h + 64) of S_i = Q_i K^T for the K tile in stage kst
-        auto issue_s_half = [&](int i, int h) {
-          const uint32_t d_tmem = tmem_base + i * 128 + h * 64;
-          const uint64_t qd = q_desc0 + static_cast<uint64_t>(i * (L::kQBytes >> 4));
-          const uint64_t kd = k_desc0 + static_cast<uint64_t>(kst * (L::kKBytes >> 4)) +
-                              static_cast<uint64_t>(h * ((64 * 128) >> 4));
-          constexpr int QC = (kTileM * 128) >> 4;  // next 64-column chunk of Q
-          constexpr int KC = (BN * 128) >> 4;      // next 64-column chunk of K
-          if constexpr (D == 128) {
-            umma_ss_group8<2, 2, 4, 4, 6, 6, QC, KC, QC + 2, KC + 2, QC + 4, KC + 4, QC + 6, KC + 6>(
-                d_tmem, qd, kd, kIdescS64, 0u);
-          } else {
-            umma_ss_group4<2, 2, 4, 4, 6, 6>(d_tmem, qd, kd, kIdescS64, 0u);
-          }
-        };
-        // keys [64h, 64h + 64) of O_i (+)= P_i V for the V tile in stage vst
-        auto issue_pv_half = [&](int i, int h, uint32_t acc0) {
-          const uint32_t d_tmem = tmem_base + 256 + i * 128;
-          const uint32_t a_tmem = tmem_base + i * 128 + h * 32;
-          const uint64_t vd = v_desc0 + static_cast<uint64_t>(vst * (L::kVBytes >> 4)) +
-                              static_cast<uint64_t>(h * ((64 * 128) >> 4));
-          constexpr int VS = (16 * 128) >> 4;  // 16 rows of V per K=16 step
-          umma_ts_group4<VS>(d_tmem, a_tmem, vd, kIdescO, acc0);
-        };
-
         int cur = 0;
         ok = next_flags(cur);
         if (ok && !(cur & kStop)) ok = start_item(cur);
@@ -1194,40 +1193,27 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
               ++mround;
             }
           }
+          if (!(me == 0 || q1)) {
+            // no block for this tile: keep the alternation
+            if (!take_turn()) { ok = false; break; }
+            pass_turn();
+          }
           if (me == 0 || q1) {
             const int i = me;
-            if constexpr (kSplitHandoff) {
-              if (!sy.warp(kSLoaded + i, sl_round[i] & 1)) { ok = false; break; }
-              ++sl_round[i];
-              tc_fence_after();
-              if (!last) issue_s_half(i, 1);
-            }
             if (!wait_o_empty(i, first)) { ok = false; break; }
-            if constexpr (kSplitHandoff) {
-              if (!sy.warp(kPHalf + i, ph_round[i] & 1)) { ok = false; break; }
-              ++ph_round[i];
-              tc_fence_after();
-              issue_pv_half(i, 0, first ? 0u : 1u);
-            }
             if (!sy.warp(kPFull + 2 * i, p_round[i] & 1)) { ok = false; break; }
             ++p_round[i];
             tc_fence_after();
-            if constexpr (kSplitHandoff) {
-              issue_pv_half(i, 1, 1u);
-            } else {
-              issue_pv(i, first, 0u);
-            }
+            if (!take_turn()) { ok = false; break; }
+            issue_pv(i, first, 0u);
             if (last) {
               umma_commit_elect(&bars[kOFull + i]);
               o_pending[i] = true;
             } else {
-              if constexpr (kSplitHandoff) {
-                issue_s_half(i, 0);
-              } else {
-                issue_s(i, 0u, 0u);
-              }
+              issue_s(i, 0u, 0u);
               umma_commit_elect(&bars[kSFull + 2 * i]);
             }
+            pass_turn();
           }
           umma_commit_elect(&bars[kVEmpty + vst]);
           advance_v();
@@ -1269,7 +1255,6 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
   int* cols = reinterpret_cast<int*>(smem + L::kCols);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int T = static_cast<int>(p.T);
   const int BM = p.block_m;
   const Sync sy{bars, abort_flag, p.timeout_ns, &p.ws->error_word, lane};
   tc_fence_before();
@@ -1380,45 +1365,25 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
       bool o_ok = true;
       if (cls == kClsF) {
         // live only for the other Q tile: contributes nothing, P = 0
-        if constexpr (kBufs<BN> == 1 && kSplitHandoff) {
-          tc_fence_before();
-          mbar_arrive(&bars[kSLoaded + wg]);
-        }
         uint32_t z[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) z[i] = 0u;
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) tmem_st16(s_cur + c * 16, z);
         tmem_st_wait();
-        if constexpr (kBufs<BN> == 1 && kSplitHandoff) {
-          tc_fence_before();
-          mbar_arrive(&bars[kPHalf + wg]);
-        }
       } else {
         // the whole S row in registers: one TMEM load, one wait
         uint32_t sr[BN];
+        const int mmode = (cls == kClsP || cls == kClsPC) ? 1 : (valid < BN ? 2 : 0);
+        float mc[kMaxChains];
+#pragma unroll
+        for (int i = 0; i < kMaxChains; ++i) mc[i] = -CUDART_INF_F;
         tmem_ld_row<BN>(s_cur, sr);
-        if constexpr (kBufs<BN> == 1 && kSplitHandoff) {
-          // S is in registers: the MMAs of the next KV tile may overwrite the
-          // upper half of these columns (P only ever occupies the lower half)
-          tc_fence_before();
-          mbar_arrive(&bars[kSLoaded + wg]);
-        }
-        if (cls == kClsP || cls == kClsPC) {
+        // masked elements to -inf, row max (two new elements per three-input max)
+        mask_and_max<0, BN>(sr, mbits, mmode, valid, mc);
+        float mt = mc[0];
 #pragma unroll
-          for (int j = 0; j < BN; ++j)
-            if ((mbits[j >> 5] >> (j & 31)) & 1u) sr[j] = __float_as_uint(-CUDART_INF_F);
-        } else if (valid < BN) {
-#pragma unroll
-          for (int j = 0; j < BN; ++j)
-            if (j >= valid) sr[j] = __float_as_uint(-CUDART_INF_F);
-        }
-        // row max, two new elements per three-input max
-        float m4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
-#pragma unroll
-        for (int j = 0; j < BN; j += 2)
-          m4[(j >> 1) & 3] = fmax3(m4[(j >> 1) & 3], __uint_as_float(sr[j]), __uint_as_float(sr[j + 1]));
-        const float mt = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+        for (int i = 1; i < kMaxChains; ++i) mt = fmaxf(mt, mc[i]);
         // scores in the log2 domain: x = s * scale * log2(e)
         const float mt2 = mt * scale_log2;
         const float m_new = fmaxf(m_run, mt2);
@@ -1435,12 +1400,12 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
         m_run = m_ref;
 
         if (__any_sync(0xffffffffu, need_o)) {
-          // rescale O before any part of this tile's P reaches a PV MMA.
-          // One S buffer: the previous PV completed before S (the lower half
-          // of S was issued after it).  Two S buffers: S was issued before
-          // the previous PV, so wait for that PV here.  Its done barrier belongs
-          // to its S buffer; the barrier's previous phase (the PV two tiles
-          // back) completed before this tile's S, so the parity is exact.
+          // rescale O before this tile's P reaches a PV MMA.  One S buffer:
+          // the previous PV completed before S, which was issued after it.
+          // Two S buffers: S was issued before the previous PV, so wait for
+          // that PV here.  Its done barrier belongs to its S buffer; the
+          // barrier's previous phase (the PV two tiles back) completed before
+          // this tile's S, so the parity is exact.
           if constexpr (kBufs<BN> == 2) {
             const uint32_t pt = n_tiles - 1u;
             o_ok = sy.warp(kPVDone + 2 * wg + (pt & 1u), (pt >> 1) & 1u);
@@ -1474,14 +1439,6 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
             pk[i >> 1] = exp2_pair_bf16(sr[j], sr[j + 1], scale2, base2, sum2[(i >> 1) & 3]);
           }
           tmem_st16(s_cur + c * 16, pk);
-          if constexpr (kBufs<BN> == 1 && kSplitHandoff) {
-            if (c == BN / 64 - 1) {
-              // the first half of P is in TMEM: its PV MMAs may start
-              tmem_st_wait();
-              tc_fence_before();
-              mbar_arrive(&bars[kPHalf + wg]);
-            }
-          }
         }
         tmem_st_wait();
         l_run += (sum_f32x2(sum2[0]) + sum_f32x2(sum2[1])) + (sum_f32x2(sum2[2]) + sum_f32x2(sum2[3]));
