@@ -62,6 +62,9 @@ constexpr int kFirstSoftmaxWarp = 4;
 constexpr int kStages = 2;
 constexpr int kTileM = 128;  // MMA M: TMEM lanes = tile rows
 constexpr int kMetaSlots = 4;
+// Interval-masked tiles whose columns form at most this many runs of equal
+// (LTS, LTE, UTS, UTE) get a run table instead of per-column tests.
+constexpr int kMaxRuns = 8;
 constexpr int kPrefetchAhead = 3;  // K/V tiles pulled into L2 ahead of their loads
 
 // With 64-column key tiles TMEM holds two S buffers per Q tile (S_i of KV
@@ -98,7 +101,8 @@ struct TileMeta {
   int c0, c1;      // key columns [c0, c1)
   int r0, r_end;   // query rows of the item [r0, r_end); tile 1 starts at r0 + block_m
   int h, kvh;      // q head, key/value head
-  int pad[7];
+  int n_runs;      // partial tiles: runs of equal intervals in the run table, 0 = per column
+  int pad[6];
 };
 static_assert(sizeof(TileMeta) == 64, "TileMeta is 64 bytes");
 
@@ -136,7 +140,9 @@ struct Layout {
   static constexpr int kV = kK + kStages * kKBytes;
   static constexpr int kCols = kV + kStages * kVBytes;  // int32 [kMetaSlots][4][BN]
   static constexpr int kMeta = kCols + kMetaSlots * 4 * BN * 4;
-  static constexpr int kBars = kMeta + kMetaSlots * static_cast<int>(sizeof(TileMeta));
+  // int32 [kMetaSlots][kMaxRuns][8]: start column, LTS, LTE, UTS, UTE of each run
+  static constexpr int kRuns = kMeta + kMetaSlots * static_cast<int>(sizeof(TileMeta));
+  static constexpr int kBars = kRuns + kMetaSlots * kMaxRuns * 8 * 4;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kEnd = kAbort + 4;
@@ -353,6 +359,13 @@ __device__ __forceinline__ void tmem_ld_row<64>(uint32_t taddr, uint32_t (&r)[64
 template <>
 __device__ __forceinline__ void tmem_ld_row<128>(uint32_t taddr, uint32_t (&r)[128]) {
   tmem_ld128(taddr, r);
+}
+
+// Bits of the columns [a, b) that fall in 32-column word w (empty if b <= a).
+__device__ __forceinline__ uint32_t range_bits(int a, int b, int w) {
+  const int lo = min(max(a - 32 * w, 0), 32);
+  const int hi = min(max(b - 32 * w, 0), 32);
+  return static_cast<uint32_t>((1ull << hi) - 1ull) & ~static_cast<uint32_t>((1ull << lo) - 1ull);
 }
 
 // max(a, b, c) in one instruction
@@ -668,6 +681,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
   TileMeta* meta = reinterpret_cast<TileMeta*>(smem + L::kMeta);
   int* cols = reinterpret_cast<int*>(smem + L::kCols);
+  int* runs = reinterpret_cast<int*>(smem + L::kRuns);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int T = static_cast<int>(p.T);
@@ -729,6 +743,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
     auto push_meta = [&](int flags, int cls0, int cls1, int c0, int c1, int r0, int r_end, int h,
                          int kvh, bool copy_cols, int mh) -> bool {
       if (!sy.warp(kMEmpty + mslot, (mround & 1) ^ 1)) return false;
+      int n_runs = 0;
       if (copy_cols) {
         const int32_t* src = p.sri + static_cast<int64_t>(mh) * 4 * p.T;
         int* dst = cols + mslot * 4 * BN;
@@ -741,9 +756,43 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
             dst[v * BN + jj] = (c < T) ? __ldg(src + static_cast<int64_t>(v) * p.T + c) : 0;
           }
         }
+        __syncwarp();
+        // runs of equal interval quadruples among the columns inside the sample
+        const int valid = c1 - c0;
+        uint32_t run_start[BN / 32];
+#pragma unroll
+        for (int m = 0; m < BN / 32; ++m) {
+          const int jj = m * 32 + lane;
+          bool st = false;
+          if (jj < valid) {
+            st = jj == 0;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) st |= jj > 0 && dst[v * BN + jj] != dst[v * BN + jj - 1];
+          }
+          run_start[m] = __ballot_sync(0xffffffffu, st);
+          n_runs += __popc(run_start[m]);
+        }
+        if (n_runs > kMaxRuns) n_runs = 0;  // per-column tests instead
+        if (n_runs > 0) {
+          int* rt = runs + mslot * kMaxRuns * 8;
+          int before = 0;
+#pragma unroll
+          for (int m = 0; m < BN / 32; ++m) {
+            const uint32_t b = run_start[m];
+            if ((b >> lane) & 1u) {
+              const int k = before + __popc(b & ((1u << lane) - 1u));
+              const int jj = m * 32 + lane;
+              rt[k * 8 + 0] = jj;
+#pragma unroll
+              for (int v = 0; v < 4; ++v) rt[k * 8 + 1 + v] = dst[v * BN + jj];
+            }
+            before += __popc(b);
+          }
+        }
       }
       if (lane == 0) {
         TileMeta& m = meta[mslot];
+        m.n_runs = n_runs;
         m.flags = flags;
         m.cls0 = cls0;
         m.cls1 = cls1;
@@ -1253,6 +1302,7 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
   TileMeta* meta = reinterpret_cast<TileMeta*>(smem + L::kMeta);
   int* cols = reinterpret_cast<int*>(smem + L::kCols);
+  const int* runs = reinterpret_cast<const int*>(smem + L::kRuns);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int BM = p.block_m;
@@ -1319,6 +1369,27 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
           const int v = valid - c * 32;     // columns from v on are outside the sample
           const uint32_t out = v >= 32 ? 0u : (v <= 0 ? 0xffffffffu : (0xffffffffu << v));
           mbits[c] = above | out;
+        }
+      } else if (cls == kClsP && meta[cur_slot].n_runs > 0) {
+        // the same rule over runs of columns with equal intervals: each run
+        // [s, e) splits at the diagonal into a lower part (masked iff
+        // LTS <= r < LTE) and an upper part (masked iff causal or
+        // UTS <= r < UTE); columns from `valid` on are outside the sample
+        const int n_runs = meta[cur_slot].n_runs;
+        const int* rt = runs + cur_slot * kMaxRuns * 8;
+        const int rr = r - c0 + 1;  // columns below rr are on or below the diagonal
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) mbits[c] = range_bits(valid, BN, c);
+        for (int k = 0; k < n_runs; ++k) {
+          const int4 ra = *reinterpret_cast<const int4*>(rt + k * 8);  // start, LTS, LTE, UTS
+          const int ute = rt[k * 8 + 4];
+          const int e = (k + 1 < n_runs) ? rt[(k + 1) * 8] : valid;
+          const bool lm = (ra.y <= r) & (r < ra.z);
+          const bool um = causal | ((ra.w <= r) & (r < ute));
+          const int mid = min(max(rr, ra.x), e);  // [s, mid) lower, [mid, e) upper
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c)
+            mbits[c] |= (lm ? range_bits(ra.x, mid, c) : 0u) | (um ? range_bits(mid, e, c) : 0u);
         }
       } else if (cls == kClsP) {
         // column intervals: row r is masked in column j iff it lies in
