@@ -14,6 +14,14 @@ reported as achieved HBM GB/s (read + write of q and k).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--configs all|headline]
+    python bench.py --sweep sparsity [--sweep-tokens T]
+
+The sparsity sweep (FlashMask article, section 4.3) times the attention call
+on one segment of T tokens whose causal-document, document or shared-question
+structure is expressed only through the column intervals, for a range of
+block sparsities rho (fully masked blocks / all blocks of the T x T grid,
+from the kernel's own block-class counts), and fits latency = a + b (1 - rho)
+per mask family.
 
 Multi-GPU (torchrun): every rank runs an independent replica of the workload
 (the path needs no exchange); value = work of all ranks / max rank time.
@@ -534,6 +542,75 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args):
+    """Latency versus block sparsity (one JSON line)."""
+    import torch
+    import packed_varlen_attention_gb300 as fm
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    T, hq, hkv, D, blk = args.sweep_tokens, 32, 8, 128, 128
+    rng = np.random.default_rng(0)
+
+    def dt(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q = dt(gen._normal_bf16(rng, (T, hq, D)))
+    k = dt(gen._normal_bf16(rng, (T, hkv, D)))
+    v = dt(gen._normal_bf16(rng, (T, hkv, D)))
+    cu_np = np.array([0, T], dtype=np.int32)
+    cu = torch.from_numpy(cu_np).to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((hq, T), dtype=torch.float32, device=dev)
+    ws = torch.empty(fm.attn_fwd_workspace_size(T, 1, hq, blk), dtype=torch.uint8, device=dev)
+    counts = torch.zeros(3, dtype=torch.int64, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    points = []
+    for family, param, causal, sri in gen.sparsity_sweep(T):
+        sri_t = torch.from_numpy(sri).to(dev)
+        mm = fm.mask_block_minmax(sri_t, cu, blk)
+
+        def call(cc=None):
+            fm.attn_fwd_varlen(q, k, v, cu, sri_t, mm, causal=causal, block_m=blk, block_n=blk,
+                               out=out, lse=lse, class_counts=cc, workspace=ws)
+
+        counts.zero_()
+        call(counts)
+        f, p_, u = (int(x) for x in counts.cpu().tolist())
+        for _ in range(args.warmup):
+            call()
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            call()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        assert fm.get_device_error(ws) == 0
+        ms = float(np.median(ts))
+        flops = 4.0 * D * hq * unmasked_pairs(cu_np, sri[0], causal)
+        points.append({"family": family, "param": param, "causal": causal,
+                       "rho": f / (f + p_ + u), "blocks_fpu": [f, p_, u], "attn_ms": ms,
+                       "effective_tflops": flops / (ms * 1e-3) / 1e12})
+    fits = {}
+    for family in sorted({pt["family"] for pt in points}):
+        xs = np.array([1.0 - pt["rho"] for pt in points if pt["family"] == family])
+        ys = np.array([pt["attn_ms"] for pt in points if pt["family"] == family])
+        A = np.stack([np.ones_like(xs), xs], axis=1)
+        coef, *_ = np.linalg.lstsq(A, ys, rcond=None)
+        resid = ys - A @ coef
+        r2 = 1.0 - float(resid @ resid) / float(((ys - ys.mean()) ** 2).sum())
+        fits[family] = {"intercept_ms": float(coef[0]), "ms_per_unit_density": float(coef[1]),
+                        "r2": r2}
+    line = {"sweep": "sparsity", "tokens": T, "heads_q": hq, "heads_kv": hkv, "head_dim": D,
+            "block": blk, "steps": args.steps, "warmup": args.warmup,
+            "l2": "flushed before every timed call (256 MiB write)", "data": "synthetic",
+            "points": points, "fits": fits}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -544,9 +621,16 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--min-warmup-seconds", type=float, default=1.0)
+    ap.add_argument("--sweep", choices=["sparsity"], default=None)
+    ap.add_argument("--sweep-tokens", type=int, default=16384)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.sweep == "sparsity":
+        if args.steps == 50:
+            args.steps = 10
+        run_sweep(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

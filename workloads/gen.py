@@ -217,6 +217,78 @@ def bidir_prefix_intervals(cu: np.ndarray, kinds, total: int, alt: bool = False)
 
 
 # ----------------------------------------------------------------------------
+# sparsity sweep (PaddleNLP FlashMask article, section 4.3): one segment of T
+# tokens, the structure expressed only through the column intervals, so every
+# block of the T x T grid is classified and the fully masked ones skipped
+# ----------------------------------------------------------------------------
+
+def single_segment_causal_documents(doc_lens) -> np.ndarray:
+    """Causal document mask over one segment: column j of a document ending at
+    e is hidden from rows [e, T); the upper triangle is causal."""
+    T = int(sum(doc_lens))
+    sri = _default_intervals(T)
+    ends = np.repeat(np.cumsum(doc_lens), doc_lens)
+    sri[0, 0, :] = ends
+    return sri
+
+
+def single_segment_documents(doc_lens) -> np.ndarray:
+    """Bidirectional document mask over one segment (non-causal): column j of
+    a document [a, e) is hidden from rows [e, T) and [0, a)."""
+    T = int(sum(doc_lens))
+    sri = _default_intervals(T)
+    cum = np.cumsum(doc_lens)
+    sri[0, 0, :] = np.repeat(cum, doc_lens)
+    sri[0, 2, :] = 0
+    sri[0, 3, :] = np.repeat(cum - np.asarray(doc_lens), doc_lens)
+    return sri
+
+
+def single_segment_shared_question(groups) -> np.ndarray:
+    """Shared-question mask over one segment (causal): ``groups`` is a list of
+    (question_len, [answer_lens]).  Question columns are hidden from rows after
+    their group; answer columns from rows after the answer (sibling answers and
+    later groups)."""
+    T = int(sum(q + sum(a) for q, a in groups))
+    sri = _default_intervals(T)
+    g0 = 0
+    for q, alens in groups:
+        gend = g0 + q + sum(alens)
+        sri[0, 0, g0:g0 + q] = gend
+        a0 = g0 + q
+        for a in alens:
+            sri[0, 0, a0:a0 + a] = a0 + a
+            a0 += a
+        g0 = gend
+    return sri
+
+
+def sparsity_sweep(T: int = 16384):
+    """The sweep's mask points: (family, parameter, causal, intervals).
+
+    causal_document / document: the segment split into n equal documents,
+    n = 1, 2, 4, ..., 64; shared_question: T / 4096 groups of one 1024-token
+    question (T / 16 in general) followed by k equal answers, k = 1, 2, 3, 4,
+    6, 8, 12.  Sparsity grows with n and with k.
+    """
+    pts = []
+    for n in (1, 2, 4, 8, 16, 32, 64):
+        if T % n:
+            continue
+        lens = [T // n] * n
+        pts.append(("causal_document", n, True, single_segment_causal_documents(lens)))
+        pts.append(("document", n, False, single_segment_documents(lens)))
+    g = T // 4
+    q = g // 4
+    for k in (1, 2, 3, 4, 6, 8, 12):
+        rest = g - q
+        alens = [rest // k] * k
+        alens[-1] += rest - sum(alens)
+        pts.append(("shared_question", k, True, single_segment_shared_question([(q, alens)] * 4)))
+    return pts
+
+
+# ----------------------------------------------------------------------------
 # tensors
 # ----------------------------------------------------------------------------
 
