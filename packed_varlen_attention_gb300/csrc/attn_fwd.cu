@@ -55,9 +55,8 @@
 namespace fm {
 namespace {
 
-// warps 0..3: K producer, MMA issuer, V producer, idle; warps 4..11: softmax
-// (two warpgroups; warp w reads TMEM lanes 32*(w%4)..+31).
-constexpr int kThreads = 384;
+// warps 0..3: K producer, MMA issuer(s), V producer; warps 4.. : one softmax
+// warpgroup per Q tile of an item (warp w reads TMEM lanes 32*(w%4)..+31).
 constexpr int kFirstSoftmaxWarp = 4;
 constexpr int kStages = 2;
 constexpr int kTileM = 128;  // MMA M: TMEM lanes = tile rows
@@ -72,13 +71,25 @@ constexpr int kPrefetchAhead = 3;  // K/V tiles pulled into L2 ahead of their lo
 // the softmax works on tile t+1) and shared memory two Q buffers (the next
 // item's Q tiles land while the current item runs).  128-column key tiles
 // fill TMEM with one S per Q tile.
-template <int BN>
-constexpr int kBufs = (BN == 64) ? 2 : 1;
+//
+// QT = Q tiles per work item (one softmax warpgroup each).  QT = 2 shares
+// every K/V tile between two Q tiles; TMEM then holds two S buffers per Q
+// tile only with 64-column key tiles.  QT = 1 leaves room for two
+// 128-column S buffers, so the single softmax warpgroup never waits for its
+// own tile's MMAs.
+template <int BN, int QT>
+constexpr int kBufs = (QT == 1 || BN == 64) ? 2 : 1;
 
 // MMA issuing warps: each Q tile has its own issuer (warps 1 and 3), so one
 // tile's barrier waits never hold up the other tile's MMAs.
-template <int BN>
-constexpr int kIssuers = 2;
+template <int QT>
+constexpr int kIssuers = QT;
+
+template <int QT>
+constexpr int kThreads = 128 + 128 * QT;
+
+// Q tiles per item for 128-column key tiles
+constexpr int kQTilesBN128 = 2;
 
 // One S buffer: the two issuers issue their blocks (PV_i of a tile and the
 // next S_i) strictly in turn, Q tile 0 first, so the tensor pipe runs one
@@ -125,18 +136,18 @@ enum Bar : int {
   kNumBars = kTurn + 2
 };
 
-// arrivals on kMEmpty: the V producer lane, the MMA issuers and the eight
-// softmax warps
-template <int BN>
-constexpr int kMEmptyCount = 9 + kIssuers<BN>;
+// arrivals on kMEmpty: the V producer lane, the MMA issuers and the softmax
+// warps
+template <int QT>
+constexpr int kMEmptyCount = 1 + kIssuers<QT> + 4 * QT;
 
-template <int D, int BN>
+template <int D, int BN, int QT>
 struct Layout {
   static constexpr int kQBytes = kTileM * D * 2;  // one Q tile
   static constexpr int kKBytes = BN * D * 2;
   static constexpr int kVBytes = BN * D * 2;
-  static constexpr int kQ = 0;  // kBufs buffers of 2 Q tiles
-  static constexpr int kK = kQ + kBufs<BN> * 2 * kQBytes;
+  static constexpr int kQ = 0;  // kBufs buffers of QT Q tiles
+  static constexpr int kK = kQ + kBufs<BN, QT> * QT * kQBytes;
   static constexpr int kV = kK + kStages * kKBytes;
   static constexpr int kCols = kV + kStages * kVBytes;  // int32 [kMetaSlots][4][BN]
   static constexpr int kMeta = kCols + kMetaSlots * 4 * BN * 4;
@@ -148,8 +159,12 @@ struct Layout {
   static constexpr int kEnd = kAbort + 4;
   static constexpr int kBytes = kEnd + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  // TMEM columns: S_i of buffer b at i*128 + b*BN (P_i packed into its first
-  // BN/2 columns), O_i at 256 + i*128.
+  // TMEM columns: S_i of buffer b at (i*kBufs + b)*BN (P_i packed into its
+  // first BN/2 columns), O_i at 256 + i*128.
+  __host__ __device__ static constexpr uint32_t s_col(int i, uint32_t b) {
+    return static_cast<uint32_t>((i * kBufs<BN, QT> + static_cast<int>(b)) * BN);
+  }
+  static_assert(QT * kBufs<BN, QT> * BN <= 256, "S buffers fit below the O columns");
   static_assert(BN <= 128 && D <= 128, "TMEM budget");
   static_assert(kBytes <= 232448, "shared memory budget");
 };
@@ -212,13 +227,13 @@ __device__ __forceinline__ int kv_tiles_to_scan(const AttnParams& p, int a, int 
 // planner: work unit = (sample, pair of consecutive Q tiles)
 // ---------------------------------------------------------------------------
 
-template <int BN>
+template <int BN, int QT>
 __global__ void __launch_bounds__(256) plan_cost_kernel(const AttnParams p) {
   const int64_t u = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (u >= p.n_qslots) return;
   const int T = static_cast<int>(p.T);
-  const int BM2 = 2 * p.block_m;
+  const int BM2 = QT * p.block_m;  // rows of one item
   int lo = 0, hi = p.n_seqs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -550,14 +565,16 @@ __device__ __forceinline__ void umma_ts_group8(uint32_t d_tmem, uint32_t a_tmem,
                : "memory");
 }
 
-// Register split between the warpgroups (all four warps of a warpgroup run
-// the same instruction).  The kernel is launched with kThreads x kLaunchRegs
-// registers; kProducerRegs x 128 + kSoftmaxRegs x 256 must not exceed that,
-// which the host checks against the compiled register count before launch.
+// Register split between the warpgroups with two Q tiles per item (all four
+// warps of a warpgroup run the same instruction).  That kernel is launched
+// with kThreads<2> x kLaunchRegs registers; kProducerRegs x 128 +
+// kSoftmaxRegs x 256 must not exceed that, which the host checks against the
+// compiled register count before launch.  With one Q tile (256 threads)
+// every warp keeps the launch budget.
 constexpr int kLaunchRegs = 168;
 constexpr int kProducerRegs = 96;
 constexpr int kSoftmaxRegs = 200;
-static_assert(kProducerRegs * 128 + kSoftmaxRegs * 256 <= kThreads * kLaunchRegs,
+static_assert(kProducerRegs * 128 + kSoftmaxRegs * 256 <= kThreads<2> * kLaunchRegs,
               "register split exceeds the launch budget");
 
 __device__ __forceinline__ void regs_release() {
@@ -580,14 +597,14 @@ __device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, i
 // ---------------------------------------------------------------------------
 
 // End of every role: all threads meet, then the warp that allocated TMEM frees it.
-template <int D, int BN>
+template <int D, int BN, int QT>
 __device__ __forceinline__ void attn_teardown(uint32_t* tmem_slot, int warp) {
   tc_fence_before();
-  asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(kThreads<QT>) : "memory");
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(*reinterpret_cast<volatile uint32_t*>(tmem_slot), Layout<D, BN>::kTmemCols);
+    tmem_dealloc(*reinterpret_cast<volatile uint32_t*>(tmem_slot), Layout<D, BN, QT>::kTmemCols);
   }
 }
 
@@ -668,11 +685,11 @@ struct Sync {
 
 // Warps 0..3 (reduced register budget): K producer, MMA issuer, V producer
 // and one idle warp; warp 0 initialises the barriers, warp 1 owns TMEM.
-template <int D, int BN, typename IdxT>
+template <int D, int BN, int QT, typename IdxT>
 __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const CUtensorMap& tq,
                                                     const CUtensorMap& tk,
                                                     const CUtensorMap& tv) {
-  using L = Layout<D, BN>;
+  using L = Layout<D, BN, QT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -690,17 +707,17 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&bars[kKFull + i], 1);
-      mbar_init(&bars[kKEmpty + i], kIssuers<BN>);
+      mbar_init(&bars[kKEmpty + i], kIssuers<QT>);
       mbar_init(&bars[kVFull + i], 1);
-      mbar_init(&bars[kVEmpty + i], kIssuers<BN>);
+      mbar_init(&bars[kVEmpty + i], kIssuers<QT>);
     }
     for (int i = 0; i < kMetaSlots; ++i) {
       mbar_init(&bars[kMFull + i], 1);
-      mbar_init(&bars[kMEmpty + i], kMEmptyCount<BN>);
+      mbar_init(&bars[kMEmpty + i], kMEmptyCount<QT>);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[kQFull + i], 1);
-      mbar_init(&bars[kQEmpty + i], kIssuers<BN>);
+      mbar_init(&bars[kQEmpty + i], kIssuers<QT>);
       mbar_init(&bars[kOFull + i], 1);
       mbar_init(&bars[kOEmpty + i], 128);
     }
@@ -828,10 +845,10 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       const int mh = p.hm > 1 ? h : 0;
       const int a = clamp_tok(__ldg(p.cu + s), T);
       const int b = max(a, clamp_tok(__ldg(p.cu + s + 1), T));
-      const int r0 = min(a + pi.y * 2 * BM, b);
+      const int r0 = min(a + pi.y * QT * BM, b);
       const int r1 = min(r0 + BM, b);
-      const int r2 = min(r0 + 2 * BM, b);
-      const bool has_q1 = r2 > r1;
+      const int r2 = min(r0 + QT * BM, b);
+      const bool has_q1 = r2 > r1;  // (never with one Q tile per item)
       const int n_kv = (b - a + BN - 1) / BN;
       const int kt_end = (r2 > r0) ? kv_tiles_to_scan<BN>(p, a, b, r2) : 0;
 
@@ -913,13 +930,13 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
           if (pushed == 0) {
             // Q tiles of this item into Q buffer q_round % kBufs, once the S
             // MMAs of the item that used that buffer last are done
-            const uint32_t qb = q_round % kBufs<BN>;
-            if (!sy.warp(kQEmpty + qb, ((q_round / kBufs<BN>) & 1) ^ 1)) {
+            const uint32_t qb = q_round % kBufs<BN, QT>;
+            if (!sy.warp(kQEmpty + qb, ((q_round / kBufs<BN, QT>) & 1) ^ 1)) {
               ok = false;
               break;
             }
             if (lane == 0) {
-              uint8_t* qdst = smem + L::kQ + qb * 2 * L::kQBytes;
+              uint8_t* qdst = smem + L::kQ + qb * QT * L::kQBytes;
               mbar_arrive_expect_tx(&bars[kQFull + qb], (has_q1 ? 2 : 1) * L::kQBytes);
 #pragma unroll
               for (int c = 0; c < D / 64; ++c)
@@ -962,7 +979,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
           mbar_wait_bounded(&bars[kKFull + st], k_armed[st] & 1, 100000000ull, nullptr);
       for (int qb = 0; qb < 2; ++qb)
         if (q_armed[qb] != 0xffffffffu)
-          mbar_wait_bounded(&bars[kQFull + qb], (q_armed[qb] / kBufs<BN>) & 1, 100000000ull,
+          mbar_wait_bounded(&bars[kQFull + qb], (q_armed[qb] / kBufs<BN, QT>) & 1, 100000000ull,
                             nullptr);
     }
     if (lane == 0 && p.class_counts != nullptr) {
@@ -973,7 +990,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       atomicAdd(reinterpret_cast<unsigned long long*>(p.class_counts + 2),
                 static_cast<unsigned long long>(cnt_u));
     }
-    attn_teardown<D, BN>(tmem_slot, warp);
+    attn_teardown<D, BN, QT>(tmem_slot, warp);
     return;
   } else if (warp == 2) {
     // --------------------------------------------------------------- V producer
@@ -1010,9 +1027,9 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
             mbar_wait_bounded(&bars[kVFull + st], v_armed[st] & 1, 100000000ull, nullptr);
       }
     }
-    attn_teardown<D, BN>(tmem_slot, warp);
+    attn_teardown<D, BN, QT>(tmem_slot, warp);
     return;
-  } else if (warp == 1 || warp == 3) {
+  } else if (warp == 1 || (warp == 3 && QT == 2)) {
     // ----------------------------------------------------------------- MMA issuers
     // The whole warp runs this loop (every branch condition is warp-uniform);
     // MMAs and commits are issued by the lane elect.sync picks.  Both issuers
@@ -1051,8 +1068,8 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       const uint64_t v_desc0 = sdesc_sw128(v_addr, BN * 128, 1024);
       // S_i = Q_i K^T for the K tile in stage kst, Q buffer qb, into S buffer sb
       auto issue_s = [&](int i, uint32_t sb, uint32_t qb) {
-        const uint32_t d_tmem = tmem_base + i * 128 + sb * BN;
-        const uint64_t qd = q_desc0 + static_cast<uint64_t>((qb * 2 + i) * (L::kQBytes >> 4));
+        const uint32_t d_tmem = tmem_base + L::s_col(i, sb);
+        const uint64_t qd = q_desc0 + static_cast<uint64_t>((qb * QT + i) * (L::kQBytes >> 4));
         const uint64_t kd = k_desc0 + static_cast<uint64_t>(kst * (L::kKBytes >> 4));
         constexpr int QC = (kTileM * 128) >> 4;  // next 64-column chunk of Q
         constexpr int KC = (BN * 128) >> 4;      // next 64-column chunk of K
@@ -1066,7 +1083,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       // O_i (+)= P_i V for the V tile in stage vst, P_i in S buffer sb
       auto issue_pv = [&](int i, bool first, uint32_t sb) {
         const uint32_t d_tmem = tmem_base + 256 + i * 128;
-        const uint32_t a_tmem = tmem_base + i * 128 + sb * BN;
+        const uint32_t a_tmem = tmem_base + L::s_col(i, sb);
         const uint64_t vd = v_desc0 + static_cast<uint64_t>(vst * (L::kVBytes >> 4));
         constexpr int VS = (16 * 128) >> 4;  // 16 rows of V per K=16 step
         if constexpr (BN == 128) {
@@ -1096,7 +1113,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         return true;
       };
 
-      if constexpr (kBufs<BN> == 2) {
+      if constexpr (kBufs<BN, QT> == 2) {
         // Two S buffers per Q tile (i = me: this issuer's tile).  The S
         // stream runs two KV tiles ahead of the PV stream: for each tile t,
         // PV_i(t) is followed by S_i(t+2),
@@ -1282,18 +1299,18 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       umma_commit_elect(&bars[kDrain + me]);
       mbar_wait_bounded(&bars[kDrain + me], 0, 100000000ull, nullptr);
     }
-    attn_teardown<D, BN>(tmem_slot, warp);
+    attn_teardown<D, BN, QT>(tmem_slot, warp);
     return;
   } else {
-    attn_teardown<D, BN>(tmem_slot, warp);  // idle warp
+    attn_teardown<D, BN, QT>(tmem_slot, warp);  // idle warp
   }
 }
 
 // Warps 4..11 (raised register budget): softmax of Q tile 0 (warps 4..7) and
 // of Q tile 1 (warps 8..11).
-template <int D, int BN, typename IdxT>
+template <int D, int BN, int QT, typename IdxT>
 __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
-  using L = Layout<D, BN>;
+  using L = Layout<D, BN, QT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1316,7 +1333,6 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
     const int wg = (warp - kFirstSoftmaxWarp) >> 2;  // which Q tile of the item
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t s_tmem = tmem_base + lane_addr + wg * 128;
     const uint32_t o_tmem = tmem_base + lane_addr + 256 + wg * 128;
     const float scale_log2 = p.scale_log2;
     const bool causal = p.causal != 0;
@@ -1427,9 +1443,9 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
       if (lane == 0) mbar_arrive(&bars[kMEmpty + cur_slot]);
 
       // S buffer of this tile and the parity of its S-full / P-full phase
-      const uint32_t sb = n_tiles % kBufs<BN>;
-      const uint32_t spar = (n_tiles / kBufs<BN>) & 1u;
-      const uint32_t s_cur = s_tmem + sb * BN;
+      const uint32_t sb = n_tiles % kBufs<BN, QT>;
+      const uint32_t spar = (n_tiles / kBufs<BN, QT>) & 1u;
+      const uint32_t s_cur = tmem_base + lane_addr + L::s_col(wg, sb);
       if (!sy.warp(kSFull + 2 * wg + sb, spar)) break;
       tc_fence_after();
 
@@ -1477,7 +1493,7 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
           // that PV here.  Its done barrier belongs to its S buffer; the
           // barrier's previous phase (the PV two tiles back) completed before
           // this tile's S, so the parity is exact.
-          if constexpr (kBufs<BN> == 2) {
+          if constexpr (kBufs<BN, QT> == 2) {
             const uint32_t pt = n_tiles - 1u;
             o_ok = sy.warp(kPVDone + 2 * wg + (pt & 1u), (pt >> 1) & 1u);
             tc_fence_after();
@@ -1521,7 +1537,7 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
       if (flags & kLast) {
         // O_i is final once the PV of this tile is done (MMAs complete in
         // issue order, so every earlier PV is done too)
-        if constexpr (kBufs<BN> == 2) {
+        if constexpr (kBufs<BN, QT> == 2) {
           if (!sy.warp(kPVDone + 2 * wg + sb, spar)) break;
         } else {
           if (!sy.warp(kOFull + wg, o_round & 1)) break;
@@ -1560,23 +1576,23 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
       }
       ++n_tiles;
     }
-    attn_teardown<D, BN>(tmem_slot, warp);
+    attn_teardown<D, BN, QT>(tmem_slot, warp);
   }
 }
 
-template <int D, int BN, typename IdxT>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int BN, int QT, typename IdxT>
+__global__ void __launch_bounds__(kThreads<QT>, 1)
     attn_fwd_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tq,
                     const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv) {
   // The register split comes first so that no value crosses from one budget
   // into the other.
   if ((threadIdx.x >> 5) < 4) {
-    regs_release();
-    attn_producer_roles<D, BN, IdxT>(p, tq, tk, tv);
+    if constexpr (QT == 2) regs_release();
+    attn_producer_roles<D, BN, QT, IdxT>(p, tq, tk, tv);
   } else {
-    regs_acquire();
-    attn_softmax_role<D, BN, IdxT>(p);
+    if constexpr (QT == 2) regs_acquire();
+    attn_softmax_role<D, BN, QT, IdxT>(p);
   }
 }
 
@@ -1593,10 +1609,10 @@ __global__ void bounded_wait_probe_kernel(int32_t* status, uint64_t timeout_ns) 
   if (threadIdx.x == 0) *status = ok ? FM_OK : FM_ERR_TIMEOUT;
 }
 
-template <int D, int BN, typename IdxT>
+template <int D, int BN, int QT, typename IdxT>
 cudaError_t launch_typed(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, int num_sms, cudaStream_t stream) {
-  using L = Layout<D, BN>;
+  using L = Layout<D, BN, QT>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1605,17 +1621,17 @@ cudaError_t launch_typed(const AttnParams& p, const CUtensorMap& tq, const CUten
     // The warpgroups' register split must fit in what the launch allocates,
     // or setmaxnreg.inc would wait forever: refuse to launch otherwise.
     cudaFuncAttributes attr;
-    e = cudaFuncGetAttributes(&attr, attn_fwd_kernel<D, BN, IdxT>);
+    e = cudaFuncGetAttributes(&attr, attn_fwd_kernel<D, BN, QT, IdxT>);
     if (e != cudaSuccess) return e;
-    if (attr.numRegs * kThreads < kProducerRegs * 128 + kSoftmaxRegs * 256)
+    if (QT == 2 && attr.numRegs * kThreads<QT> < kProducerRegs * 128 + kSoftmaxRegs * 256)
       return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(attn_fwd_kernel<D, BN, IdxT>,
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D, BN, QT, IdxT>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
     if (dev < 64) configured |= 1ull << dev;
   }
   const int64_t n_slots = p.n_qslots;
-  plan_cost_kernel<BN><<<static_cast<unsigned>((n_slots + 7) / 8), 256, 0, stream>>>(p);
+  plan_cost_kernel<BN, QT><<<static_cast<unsigned>((n_slots + 7) / 8), 256, 0, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   plan_order_kernel<<<1, kCostBins, 0, stream>>>(p);
@@ -1623,7 +1639,7 @@ cudaError_t launch_typed(const AttnParams& p, const CUtensorMap& tq, const CUten
   if (e != cudaSuccess) return e;
   const int64_t max_items = n_slots * p.hq;
   const int grid = static_cast<int>(max_items < num_sms ? max_items : num_sms);
-  attn_fwd_kernel<D, BN, IdxT><<<grid, kThreads, L::kBytes, stream>>>(p, tq, tk, tv);
+  attn_fwd_kernel<D, BN, QT, IdxT><<<grid, kThreads<QT>, L::kBytes, stream>>>(p, tq, tk, tv);
   return cudaGetLastError();
 }
 
@@ -1641,16 +1657,16 @@ cudaError_t launch_attn_fwd(const AttnParams& p, const CUtensorMap& tq, const CU
                             cudaStream_t stream) {
   if (p.head_dim == 128) {
     if (p.block_n == 128)
-      return use_int64 ? launch_typed<128, 128, int64_t>(p, tq, tk, tv, num_sms, stream)
-                       : launch_typed<128, 128, int32_t>(p, tq, tk, tv, num_sms, stream);
-    return use_int64 ? launch_typed<128, 64, int64_t>(p, tq, tk, tv, num_sms, stream)
-                     : launch_typed<128, 64, int32_t>(p, tq, tk, tv, num_sms, stream);
+      return use_int64 ? launch_typed<128, 128, kQTilesBN128, int64_t>(p, tq, tk, tv, num_sms, stream)
+                       : launch_typed<128, 128, kQTilesBN128, int32_t>(p, tq, tk, tv, num_sms, stream);
+    return use_int64 ? launch_typed<128, 64, 2, int64_t>(p, tq, tk, tv, num_sms, stream)
+                     : launch_typed<128, 64, 2, int32_t>(p, tq, tk, tv, num_sms, stream);
   }
   if (p.block_n == 128)
-    return use_int64 ? launch_typed<64, 128, int64_t>(p, tq, tk, tv, num_sms, stream)
-                     : launch_typed<64, 128, int32_t>(p, tq, tk, tv, num_sms, stream);
-  return use_int64 ? launch_typed<64, 64, int64_t>(p, tq, tk, tv, num_sms, stream)
-                   : launch_typed<64, 64, int32_t>(p, tq, tk, tv, num_sms, stream);
+    return use_int64 ? launch_typed<64, 128, kQTilesBN128, int64_t>(p, tq, tk, tv, num_sms, stream)
+                     : launch_typed<64, 128, kQTilesBN128, int32_t>(p, tq, tk, tv, num_sms, stream);
+  return use_int64 ? launch_typed<64, 64, 2, int64_t>(p, tq, tk, tv, num_sms, stream)
+                   : launch_typed<64, 64, 2, int32_t>(p, tq, tk, tv, num_sms, stream);
 }
 
 cudaError_t launch_bounded_wait_probe(int32_t* status, uint64_t timeout_ns, cudaStream_t stream) {
