@@ -19,7 +19,8 @@ Sources, cited by page title and section:
   ``R = [[0, I], [-I, 0]]``, and the backward rule ``sin -> -sin``);
   section "Uncontaminated packing" (positions reset for every packed
   sample); section "Why padding is needed and the maths of the speedup".
-* "PaddleNLP FlashMask in practice" article: section 2.1 (column-wise
+* "PaddleNLP FlashMask in practice" article: section 3.4 (the backward
+  operator's inputs and outputs); section 2.1 (column-wise
   intervals ``[start_j, end_j)``), section 2.2 (the LTS/LTE/UTS/UTE vectors,
   their defaults and the 16x16 causal example), section 3.1 (the eight
   per-tile min/max vectors), section 3.2 (the three block classes), section
@@ -43,6 +44,9 @@ Parity status per function (what pins it, besides itself):
 * ``attention.attention_forward``: pinned (single key, textbook softmax via
   scipy, brute-force loop on tiny inputs, encoding invariants).
 * ``packing``: pinned (the printed closed forms and token / CTA counts).
+* ``attention_bwd.attention_backward``: pinned (central finite differences of
+  ``attention_forward`` for six mask styles with GQA, fully masked rows, a
+  closed form); ``attention_bwd.row_delta``: pinned (sum of p times dp).
 """
 
-from . import attention, mask, packing, rope  # noqa: F401
+from . import attention, attention_bwd, mask, packing, rope  # noqa: F401
