@@ -231,6 +231,58 @@ FM_API fm_status fm_attn_fwd_varlen_noalloc(const void* q, const void* k, const 
                                             void* stream);
 
 /*
+ * fm_attn_bwd_workspace_size -- bytes of device workspace that
+ * fm_attn_bwd_varlen needs: a 256-byte header (counters, device error word)
+ * and two float arrays of Hq * T.  Returns 0 on invalid arguments.
+ */
+FM_API size_t fm_attn_bwd_workspace_size(int64_t total_tokens, int n_heads_q);
+
+/*
+ * fm_attn_bwd_varlen -- FlashMask attention backward over packed samples.
+ *
+ * PaddleNLP FlashMask article, section 3.4: the backward operator takes q,
+ * k, v, the column intervals, out, softmax_lse and the gradient of out, and
+ * returns the gradients of q, k and v; section 3.3: the block-skipping
+ * kernel equals dense-mask attention, so these are the gradients of the
+ * attention defined at fm_attn_fwd_varlen (same mask rules).  With
+ * p_ij = exp(scale * q_i . k_j - lse_i) over unmasked pairs of a sample,
+ * delta_i = dout_i . out_i and ds_ij = p_ij (dout_i . v_j - delta_i):
+ *     dq_i = scale * sum_j ds_ij k_j
+ *     dk_j = scale * sum over q heads of the group and rows i of ds_ij q_i
+ *     dv_j = sum over q heads of the group and rows i of p_ij dout_i
+ * Rows with lse = -inf (no unmasked key) contribute nothing.  Fully masked
+ * blocks are skipped using the block statistics (section 3.2).  Every
+ * gradient row is owned by one CTA (no atomics): results are bitwise
+ * reproducible from run to run.
+ *
+ *   q, k, v, cu_seqlens, n_heads_q, n_heads_kv, head_dim,
+ *   startend_row_indices, n_mask_heads, causal, softmax_scale: as for
+ *                     fm_attn_fwd_varlen (the values of the forward call).
+ *   out, lse          device outputs of that forward call: bf16 [T][Hq][D]
+ *                     and float [Hq][T].
+ *   dout              device bf16 [T][Hq][D], 16-byte aligned.
+ *   block_minmax      device output of fm_mask_block_minmax with block_n =
+ *                     128 (NULL when startend_row_indices is NULL).
+ *   dq                device bf16 [T][Hq][D] (written).
+ *   dk, dv            device bf16 [T][Hkv][D] (written).
+ *   workspace         device buffer of workspace_bytes >=
+ *                     fm_attn_bwd_workspace_size(T, Hq), 256-byte aligned; no
+ *                     initialisation needed.  Calls that share a workspace
+ *                     must be ordered on one stream.  fm_get_device_error
+ *                     reads its error word.
+ *   flags             FM_FLAG_FORCE_INT64 or 0.
+ * Pointers to tensors must be 16-byte aligned, lse 4-byte aligned.
+ */
+FM_API fm_status fm_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* out,
+                                    const void* dout, const float* lse, int64_t total_tokens,
+                                    int n_heads_q, int n_heads_kv, int head_dim,
+                                    const int32_t* cu_seqlens, int n_seqs,
+                                    const int32_t* startend_row_indices, int n_mask_heads,
+                                    const int32_t* block_minmax, int causal, float softmax_scale,
+                                    void* dq, void* dk, void* dv, void* workspace,
+                                    size_t workspace_bytes, uint32_t flags, void* stream);
+
+/*
  * fm_attn_fwd_num_work_items -- after fm_attn_fwd_varlen has completed on
  * `stream`, copies to *host_items the number of work items its scheduler
  * built (real Q tiles times Hq).  Synchronises `stream`.
@@ -239,8 +291,8 @@ FM_API fm_status fm_attn_fwd_num_work_items(const void* workspace, int64_t* host
 
 /*
  * fm_get_device_error -- synchronises `stream` and copies the device error
- * word of the last fm_attn_fwd_varlen that used `workspace` into *host_err
- * (a bit set of FM_DEVERR_*; 0 when clean).
+ * word of the last fm_attn_fwd_varlen or fm_attn_bwd_varlen that used
+ * `workspace` into *host_err (a bit set of FM_DEVERR_*; 0 when clean).
  */
 FM_API fm_status fm_get_device_error(const void* workspace, int32_t* host_err, void* stream);
 

@@ -38,8 +38,18 @@ from .mask import dense_mask
 
 def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray,
                        cu_seqlens: np.ndarray, sri: Optional[np.ndarray], causal: bool,
-                       scale: Optional[float] = None):
-    """Returns (dq [T, Hq, D], dk [T, Hkv, D], dv [T, Hkv, D]) in float64."""
+                       scale: Optional[float] = None, magnitudes: bool = False):
+    """Returns (dq [T, Hq, D], dk [T, Hkv, D], dv [T, Hkv, D]) in float64.
+
+    With ``magnitudes=True`` also returns the magnitude sums (mq, mk, mv) of
+    the same shapes that bound how far rounded arithmetic can stray from
+    these values (used only to derive test tolerances):
+        e_i  = sum_d |do_id| (sum_j p_ij |v_jd|)
+        mv_j = sum_i p_ij |do_i|
+        mk_j = scale * sum_i (|ds_ij| + p_ij e_i) |q_i|
+        mq_i = scale * sum_j (|ds_ij| + p_ij e_i) |k_j|
+    summed over the q heads of a key/value head like the gradients.
+    """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
@@ -53,6 +63,10 @@ def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.nda
     dq = np.zeros((T, Hq, D))
     dk = np.zeros((T, Hkv, D))
     dv = np.zeros((T, Hkv, D))
+    if magnitudes:
+        mq = np.zeros((T, Hq, D))
+        mk = np.zeros((T, Hkv, D))
+        mv = np.zeros((T, Hkv, D))
     for s in range(len(cu) - 1):
         a, b = int(cu[s]), int(cu[s + 1])
         if b <= a:
@@ -78,6 +92,14 @@ def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.nda
             dv[a:b, g, :] += p.T @ do[a:b, h, :]
             dq[a:b, h, :] = scale * (ds @ k[a:b, g, :])
             dk[a:b, g, :] += scale * (ds.T @ q[a:b, h, :])
+            if magnitudes:
+                eo = (np.abs(do[a:b, h, :]) * (p @ np.abs(v[a:b, g, :]))).sum(axis=1)
+                w = np.abs(ds) + p * eo[:, None]
+                mv[a:b, g, :] += p.T @ np.abs(do[a:b, h, :])
+                mk[a:b, g, :] += scale * (w.T @ np.abs(q[a:b, h, :]))
+                mq[a:b, h, :] = scale * (w @ np.abs(k[a:b, g, :]))
+    if magnitudes:
+        return dq, dk, dv, mq, mk, mv
     return dq, dk, dv
 
 

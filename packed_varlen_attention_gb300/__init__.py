@@ -11,6 +11,7 @@ Entry points (same names as the C ABI in ``include/fm.h``):
 * ``rope_qk_varlen``       fused in-place QK RoPE, positions reset per sample
 * ``mask_block_minmax``    FlashMask per-key-tile min/max of LTS/LTE/UTS/UTE
 * ``attn_fwd_varlen``      FlashMask attention forward (out, lse)
+* ``attn_bwd_varlen``      FlashMask attention backward (dq, dk, dv)
 """
 
 from __future__ import annotations
@@ -30,6 +31,8 @@ __all__ = [
     "attn_fwd_varlen",
     "attn_fwd_varlen_noalloc",
     "attn_fwd_num_work_items",
+    "attn_bwd_workspace_size",
+    "attn_bwd_varlen",
     "get_device_error",
     "debug_bounded_wait",
     "status_string",
@@ -67,6 +70,11 @@ _SIGNATURES = {
                                             ctypes.c_float, _c_int, _c_int, _c_vp, _c_vp, _c_vp,
                                             _c_u32, _c_vp]),
     "fm_attn_fwd_num_work_items": (_c_int, [_c_vp, ctypes.POINTER(_c_i64), _c_vp]),
+    "fm_attn_bwd_workspace_size": (ctypes.c_size_t, [_c_i64, _c_int]),
+    "fm_attn_bwd_varlen": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_int,
+                                    _c_int, _c_int, _c_vp, _c_int, _c_vp, _c_int, _c_vp, _c_int,
+                                    ctypes.c_float, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t,
+                                    _c_u32, _c_vp]),
     "fm_get_device_error": (_c_int, [_c_vp, ctypes.POINTER(ctypes.c_int32), _c_vp]),
     "fm_debug_bounded_wait": (_c_int, [_c_vp, ctypes.c_uint64, _c_vp]),
     "fm_status_string": (ctypes.c_char_p, [_c_int]),
@@ -265,6 +273,55 @@ def attn_fwd_varlen_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
         int(bool(causal)), float(softmax_scale), block_m, block_n, _ptr(out), _ptr(lse),
         _ptr(class_counts), FM_FLAG_FORCE_INT64 if force_int64 else 0, _stream(stream)))
     return out, lse
+
+
+def attn_bwd_workspace_size(total_tokens: int, n_heads_q: int) -> int:
+    return int(_lib().fm_attn_bwd_workspace_size(total_tokens, n_heads_q))
+
+
+def attn_bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
+                    dout: torch.Tensor, lse: torch.Tensor, cu_seqlens: torch.Tensor,
+                    startend_row_indices: Optional[torch.Tensor] = None,
+                    block_minmax: Optional[torch.Tensor] = None, causal: bool = False,
+                    softmax_scale: float = 0.0, dq: Optional[torch.Tensor] = None,
+                    dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
+                    workspace: Optional[torch.Tensor] = None, force_int64: bool = False,
+                    stream=None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """FlashMask attention backward. Returns (dq, dk, dv), bf16, shaped like q, k, v.
+
+    ``block_minmax`` must come from ``mask_block_minmax(..., block_n=128)``.
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _need(t, n, torch.bfloat16)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous [T, H, D]")
+    _need(lse, "lse", torch.float32)
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    T, hq, d = q.shape
+    hkv = k.shape[1]
+    n_seqs = cu_seqlens.numel() - 1
+    hm = 0
+    if startend_row_indices is not None:
+        _need(startend_row_indices, "startend_row_indices", torch.int32)
+        hm = startend_row_indices.shape[0]
+        if block_minmax is None:
+            raise ValueError("block_minmax (from mask_block_minmax, block_n=128) is required")
+        _need(block_minmax, "block_minmax", torch.int32)
+    if dq is None:
+        dq = torch.empty_like(q)
+    if dk is None:
+        dk = torch.empty_like(k)
+    if dv is None:
+        dv = torch.empty_like(v)
+    if workspace is None:
+        workspace = torch.empty(attn_bwd_workspace_size(T, hq), dtype=torch.uint8,
+                                device=q.device)
+    _check("fm_attn_bwd_varlen", _lib().fm_attn_bwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), T, hq, hkv, d,
+        _ptr(cu_seqlens), n_seqs, _ptr(startend_row_indices), hm, _ptr(block_minmax),
+        int(bool(causal)), float(softmax_scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+        workspace.numel(), FM_FLAG_FORCE_INT64 if force_int64 else 0, _stream(stream)))
+    return dq, dk, dv
 
 
 def attn_fwd_num_work_items(workspace: torch.Tensor, stream=None) -> int:

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libfm.so")
-SOURCES = ["rope_varlen.cu", "mask_minmax.cu", "attn_fwd.cu", "fm_api.cu", "attn_fwd_noalloc.cu"]
+SOURCES = ["rope_varlen.cu", "mask_minmax.cu", "attn_fwd.cu", "attn_bwd.cu", "fm_api.cu", "attn_fwd_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 

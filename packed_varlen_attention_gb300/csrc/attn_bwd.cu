@@ -1,0 +1,960 @@
+// attn_bwd.cu -- FlashMask attention backward over packed samples on sm_103a.
+//
+// What is computed (PaddleNLP FlashMask article, section 3.4: the backward
+// operator takes q, k, v, the column intervals, out, softmax_lse and the
+// output gradient; section 3.3: the block-skipping kernel equals dense-mask
+// attention, so its gradient is the gradient of dense-mask attention).  For
+// every sample, q head h (key/value head g = h / (Hq / Hkv)) and unmasked
+// pair (i, j):
+//     p_ij  = exp(scale * q_i . k_j - lse_i)      (lse from the forward pass)
+//     dp_ij = do_i . v_j,   delta_i = do_i . o_i
+//     ds_ij = p_ij * (dp_ij - delta_i)
+//     dq_i  = scale * sum_j ds_ij k_j
+//     dk_j  = scale * sum_{h in group, i} ds_ij q_i
+//     dv_j  = sum_{h in group, i} p_ij do_i
+// The same block classes as the forward pass (section 3.2) skip fully masked
+// blocks and restrict the element mask to partially masked ones.
+//
+// How it runs on GB300 -- three launches, every sum owned by one CTA (no
+// atomics, so the gradients are bitwise reproducible):
+//   * prep: one pass over out and dout: -delta_i and -lse_i * log2(e) per
+//     (head, row) into the workspace (fp32).
+//   * dK/dV kernel: a work item is one 128-key tile of one key/value head;
+//     it walks every q head of the group and every 64-row Q tile that is not
+//     fully masked, keeping dK and dV in TMEM for the whole item.
+//   * dQ kernel: a work item is one 128-row Q tile of one q head; it walks
+//     the 64-key tiles that are not fully masked, keeping dQ in TMEM.
+// Both are one persistent kernel template (one CTA per SM pulling items from
+// an atomic counter) with the same warp roles (256 threads):
+//   warp 0   producer: block classes of the item's steps, per-step metadata
+//            in an 8-slot ring, TMA loads of the two resident tiles (R1, R2:
+//            K, V or Q, dO; 128 rows) once per item and of the first
+//            streamed tile (C1: Q or K; 64 rows) per step;
+//   warp 2   TMA loads of the second streamed tile (C2: dO or V) per step;
+//   warp 1   MMA issuer (whole warp converged, elect.sync picks the lane):
+//            X = R1 C1^T and Y = R2 C2^T (tcgen05.mma kind::f16, M = 128,
+//            N = 64, fp32 in TMEM, two buffers), then with operand A read
+//            from TMEM: dV += P^T dO and dK += dS^T Q, or dQ += dS K;
+//   warps 4..7  elementwise, one thread per TMEM lane: masks X, forms
+//            P = 2^(X * scale * log2 e - lse * log2 e) and
+//            dS = P * (Y - delta), stores them as bf16 into TMEM over X and
+//            Y, and writes the gradients of the item at its end.
+// The X/Y stream runs two steps ahead of the accumulating MMAs, so the
+// elementwise warps work on step t while the tensor cores run step t+1.
+// Every mbarrier wait is bounded and reports FM_DEVERR_TIMEOUT instead of
+// hanging.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "attn_common.cuh"
+#include "fm_device.cuh"
+#include "fm_internal.h"
+
+namespace fm {
+namespace {
+
+enum : int { kModeDQ = 0, kModeDKV = 1 };
+
+constexpr int kBwdThreads = 256;
+constexpr int kRes = 128;       // resident tile rows = TMEM lanes
+constexpr int kSub = 64;        // streamed tile rows
+constexpr int kStatTile = 128;  // key tile of the block statistics
+constexpr int kBwdMeta = 8;     // metadata ring slots
+constexpr int kSlotBytes = 1024;
+constexpr int kMaxStages = 8;
+
+template <int D>
+constexpr int kBwdStages = D == 128 ? 4 : 6;
+
+enum : int { kFirst = 1, kLast = 2, kStop = 8 };
+
+struct BwdMeta {
+  int flags;  // kFirst | kLast, or kStop
+  int cls;    // block class of this step
+  int c0;     // first row (token) of the streamed tile
+  int r0;     // first row (token) of the resident tile
+  int b;      // end of the sample
+  int h;      // q head of this step
+  int kvh;    // key/value head
+  int mh;     // mask head
+  int pad[8];
+};
+static_assert(sizeof(BwdMeta) == 64, "BwdMeta is 64 bytes");
+
+enum BwdBar : int {
+  bC1Full = 0,
+  bC1Empty = bC1Full + kMaxStages,
+  bC2Full = bC1Empty + kMaxStages,
+  bC2Empty = bC2Full + kMaxStages,
+  bMFull = bC2Empty + kMaxStages,
+  bMEmpty = bMFull + kBwdMeta,
+  bRFull = bMEmpty + kBwdMeta,  // both resident tiles of an item landed
+  bREmpty,                      // last X/Y MMAs of an item done
+  bSFull,                       // [2 buffers] X and Y ready
+  bPFull = bSFull + 2,          // [2 buffers] P / dS written (128 arrivals)
+  bAccFull = bPFull + 2,        // last accumulating MMA of an item done
+  bAccEmpty,                    // accumulators read by the epilogue (128 arrivals)
+  bDrain,
+  bNumBars
+};
+
+// arrivals on bMEmpty: the issuer, the C2 producer and the four elementwise warps
+constexpr int kBwdMEmptyCount = 6;
+
+template <int D>
+struct BwdLayout {
+  static constexpr int NS = kBwdStages<D>;
+  static constexpr int kRBytes = kRes * D * 2;
+  static constexpr int kCBytes = kSub * D * 2;
+  static constexpr int kR = 0;  // R1, then R2
+  static constexpr int kC1 = 2 * kRBytes;
+  static constexpr int kC2 = kC1 + NS * kCBytes;
+  static constexpr int kSlots = kC2 + NS * kCBytes;  // per-step data, kSlotBytes each
+  static constexpr int kMeta = kSlots + kBwdMeta * kSlotBytes;
+  static constexpr int kBars = kMeta + kBwdMeta * static_cast<int>(sizeof(BwdMeta));
+  static constexpr int kTmemSlot = kBars + bNumBars * 8;
+  static constexpr int kAbort = kTmemSlot + 4;
+  static constexpr int kEnd = kAbort + 4;
+  static constexpr int kBytes = kEnd + 1024;  // + alignment slack
+  static constexpr uint32_t kTmemCols = 512;
+  // TMEM columns: X of buffer b at 64 b (P over its first 32), Y at
+  // 128 + 64 b (dS over its first 32), accumulators at 256 (dQ or dV) and
+  // 256 + D (dK).
+  __host__ __device__ static constexpr uint32_t x_col(uint32_t b) { return 64u * b; }
+  __host__ __device__ static constexpr uint32_t y_col(uint32_t b) { return 128u + 64u * b; }
+  static constexpr uint32_t kAcc0 = 256;
+  static constexpr uint32_t kAcc1 = 256 + D;
+  static_assert(NS <= kMaxStages, "stage barriers");
+  static_assert(kBytes <= 232448, "shared memory budget");
+  static_assert(kSub * 4 * 4 <= kSlotBytes, "slot holds four interval vectors");
+};
+
+// sample of packed tile slot u (slots: floor(cu[s] / tile) + s + t)
+__device__ __forceinline__ int slot_sample(const AttnBwdParams& p, int64_t u, int tile) {
+  const int T = static_cast<int>(p.T);
+  int lo = 0, hi = p.n_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    const int64_t base = static_cast<int64_t>(clamp_tok(__ldg(p.cu + mid), T)) / tile + mid;
+    if (base <= u) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ void load_stats(const AttnBwdParams& p, int mh, int64_t slot,
+                                           int (&st)[8]) {
+#pragma unroll
+  for (int v = 0; v < 8; ++v)
+    st[v] = __ldg(p.minmax + (static_cast<int64_t>(mh) * 8 + v) * p.n_kv_slots + slot);
+}
+
+// P and dS for two elements: p = 2^(x * c + nl), ds = p * (y + nd); returns
+// both as bf16x2 (first element in the low half).
+__device__ __forceinline__ void bwd_pair(uint32_t x0, uint32_t x1, uint32_t y0, uint32_t y1,
+                                         uint64_t c2, uint64_t nl2, uint64_t nd2, uint32_t& pk,
+                                         uint32_t& dsk) {
+  asm("{\n\t.reg .b64 x, e, p, y, t;\n\t.reg .f32 e0, e1, p0, p1, t0, t1;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "fma.rn.f32x2 e, x, %6, %7;\n\t"
+      "mov.b64 {e0, e1}, e;\n\t"
+      "ex2.approx.ftz.f32 p0, e0;\n\t"
+      "ex2.approx.ftz.f32 p1, e1;\n\t"
+      "mov.b64 p, {p0, p1};\n\t"
+      "mov.b64 y, {%4, %5};\n\t"
+      "add.f32x2 t, y, %8;\n\t"
+      "mul.f32x2 t, t, p;\n\t"
+      "mov.b64 {t0, t1}, t;\n\t"
+      "cvt.rn.bf16x2.f32 %0, p1, p0;\n\t"
+      "cvt.rn.bf16x2.f32 %1, t1, t0;\n\t}"
+      : "=r"(pk), "=r"(dsk)
+      : "r"(x0), "r"(x1), "r"(y0), "r"(y1), "l"(c2), "l"(nl2), "l"(nd2));
+}
+
+// ---------------------------------------------------------------------------
+// prep: -delta and -lse * log2(e)
+// ---------------------------------------------------------------------------
+
+// One group of D/8 threads per (token, head) row, 8 elements per thread.
+template <int D, typename IdxT>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const AttnBwdParams p) {
+  constexpr int G = D / 8;
+  const int64_t n_rows = p.T * p.hq;
+  const int64_t r = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) / G;
+  const int part = threadIdx.x % G;
+  float acc = 0.f;
+  if (r < n_rows) {
+    const uint4 o4 = __ldg(reinterpret_cast<const uint4*>(
+                               static_cast<const __nv_bfloat16*>(p.out) + static_cast<IdxT>(r) * D) +
+                           part);
+    const uint4 d4 = __ldg(reinterpret_cast<const uint4*>(
+                               static_cast<const __nv_bfloat16*>(p.dout) + static_cast<IdxT>(r) * D) +
+                           part);
+    const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w};
+    const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[u]));
+      const float2 df = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dw[u]));
+      acc = fmaf(of.x, df.x, acc);
+      acc = fmaf(of.y, df.y, acc);
+    }
+  }
+#pragma unroll
+  for (int d = G / 2; d > 0; d >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, d);
+  if (r < n_rows && part == 0) {
+    const int64_t t = r / p.hq;
+    const int h = static_cast<int>(r % p.hq);
+    const IdxT o = static_cast<IdxT>(h) * static_cast<IdxT>(p.T) + static_cast<IdxT>(t);
+    const float l = __ldg(p.lse + o);
+    p.ndelta[o] = -acc;
+    p.nlse2[o] = (l == -CUDART_INF_F) ? -CUDART_INF_F : -l * 1.4426950408889634f;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dK/dV and dQ kernels
+// ---------------------------------------------------------------------------
+
+template <int D>
+__device__ __forceinline__ void bwd_teardown(uint32_t* tmem_slot, int warp) {
+  tc_fence_before();
+  asm volatile("bar.sync 1, %0;" ::"n"(kBwdThreads) : "memory");
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(*reinterpret_cast<volatile uint32_t*>(tmem_slot), BwdLayout<D>::kTmemCols);
+  }
+}
+
+// Zero gradients of resident rows [r0, r1) (an item none of whose blocks is
+// live): dq of head h, or dk and dv of head h.
+template <int D, int Mode, typename IdxT>
+__device__ __forceinline__ void zero_rows(const AttnBwdParams& p, int r0, int r1, int h,
+                                          int lane) {
+  const int heads = Mode == kModeDQ ? p.hq : p.hkv;
+  for (int r = r0 + lane; r < r1; r += 32) {
+    const IdxT off = (static_cast<IdxT>(r) * heads + h) * static_cast<IdxT>(D);
+    uint4* d0 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(Mode == kModeDQ ? p.dq : p.dv) + off);
+#pragma unroll
+    for (int u = 0; u < D / 8; ++u) d0[u] = make_uint4(0u, 0u, 0u, 0u);
+    if (Mode == kModeDKV) {
+      uint4* d1 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dk) + off);
+#pragma unroll
+      for (int u = 0; u < D / 8; ++u) d1[u] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+}
+
+// Rows [r0, r1) and columns [c0, c1) of a (query rows, key columns) block.
+__device__ __forceinline__ int block_class(const AttnBwdParams& p, const int (&st)[8], int q0,
+                                           int q1, int k0, int k1) {
+  return classify_block(q0, q1, k0, k1, st, p.sri != nullptr, p.causal != 0);
+}
+
+template <int D, int Mode, typename IdxT>
+__device__ __forceinline__ void bwd_producer_roles(const AttnBwdParams& p, const CUtensorMap& tr1,
+                                                   const CUtensorMap& tr2, const CUtensorMap& tc1,
+                                                   const CUtensorMap& tc2) {
+  using L = BwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
+  BwdMeta* meta = reinterpret_cast<BwdMeta*>(smem + L::kMeta);
+  uint8_t* slots = smem + L::kSlots;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int T = static_cast<int>(p.T);
+  const Sync sy{bars, abort_flag, p.timeout_ns, &p.ws->error_word, lane};
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::NS; ++i) {
+      mbar_init(&bars[bC1Full + i], 1);
+      mbar_init(&bars[bC1Empty + i], 1);
+      mbar_init(&bars[bC2Full + i], 1);
+      mbar_init(&bars[bC2Empty + i], 1);
+    }
+    for (int i = 0; i < kBwdMeta; ++i) {
+      mbar_init(&bars[bMFull + i], 1);
+      mbar_init(&bars[bMEmpty + i], kBwdMEmptyCount);
+    }
+    mbar_init(&bars[bRFull], 1);
+    mbar_init(&bars[bREmpty], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[bSFull + i], 1);
+      mbar_init(&bars[bPFull + i], 128);
+    }
+    mbar_init(&bars[bAccFull], 1);
+    mbar_init(&bars[bAccEmpty], 128);
+    mbar_init(&bars[bDrain], 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+    tma_prefetch_desc(&tr1);
+    tma_prefetch_desc(&tr2);
+    tma_prefetch_desc(&tc1);
+    tma_prefetch_desc(&tc2);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------- producer + metadata
+    const int group = p.hq / p.hkv;
+    const int n_heads_item = Mode == kModeDQ ? p.hq : p.hkv;
+    const int64_t n_items = p.n_res_slots * n_heads_item;
+    uint32_t* counter = Mode == kModeDQ ? &p.ws->work_counter : &p.ws->work_counter_kv;
+    uint32_t mslot = 0, mround = 0;
+    uint32_t cst = 0, cround = 0;
+    uint32_t r_round = 0;
+    uint32_t c_armed[kMaxStages];
+#pragma unroll
+    for (int i = 0; i < kMaxStages; ++i) c_armed[i] = 0xffffffffu;
+    uint32_t r_armed = 0xffffffffu;
+    bool ok = true;
+
+    auto push_meta = [&](int flags, int cls, int c0, int r0, int b, int h, int kvh,
+                         int mh) -> bool {
+      if (!sy.warp(bMEmpty + mslot, (mround & 1) ^ 1)) return false;
+      if (!(flags & kStop)) {
+        uint8_t* sd = slots + mslot * kSlotBytes;
+        if (Mode == kModeDQ) {
+          if (cls == kClsP) {
+            // the four interval vectors of the 64 key columns
+            int* cl = reinterpret_cast<int*>(sd);
+            const int32_t* src = p.sri + static_cast<int64_t>(mh) * 4 * p.T;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+#pragma unroll
+              for (int m = 0; m < kSub / 32; ++m) {
+                const int jj = m * 32 + lane;
+                const int c = c0 + jj;
+                cl[v * kSub + jj] =
+                    (c < b && c < T) ? __ldg(src + static_cast<int64_t>(v) * p.T + c) : 0;
+              }
+            }
+          }
+        } else {
+          // -lse*log2(e) and -delta of the 64 query rows; rows outside the
+          // sample get -inf (p = 0 without a mask test) and 0
+          float* nl = reinterpret_cast<float*>(sd);
+          float* nd = nl + kSub;
+#pragma unroll
+          for (int m = 0; m < kSub / 32; ++m) {
+            const int jj = m * 32 + lane;
+            const int i = c0 + jj;
+            float a = -CUDART_INF_F, d = 0.f;
+            if (i < b && i < T) {
+              const IdxT o = static_cast<IdxT>(h) * static_cast<IdxT>(p.T) + static_cast<IdxT>(i);
+              a = __ldg(p.nlse2 + o);
+              d = __ldg(p.ndelta + o);
+            }
+            nl[jj] = a;
+            nd[jj] = d;
+          }
+        }
+      }
+      if (lane == 0) {
+        BwdMeta& m = meta[mslot];
+        m.flags = flags;
+        m.cls = cls;
+        m.c0 = c0;
+        m.r0 = r0;
+        m.b = b;
+        m.h = h;
+        m.kvh = kvh;
+        m.mh = mh;
+      }
+      __threadfence_block();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[bMFull + mslot]);
+      if (++mslot == kBwdMeta) {
+        mslot = 0;
+        ++mround;
+      }
+      return true;
+    };
+
+    // one step: metadata, the resident tiles (first step), the C1 tile
+    auto push_step = [&](int flags, int cls, int c0, int r0, int b, int h, int kvh,
+                         int mh) -> bool {
+      if (!push_meta(flags, cls, c0, r0, b, h, kvh, mh)) return false;
+      if (flags & kFirst) {
+        if (!sy.warp(bREmpty, (r_round & 1) ^ 1)) return false;
+        if (lane == 0) {
+          const int rx = (Mode == kModeDQ ? h : kvh) * D;
+          mbar_arrive_expect_tx(&bars[bRFull], 2 * L::kRBytes);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_2d(smem + L::kR + c * (kRes * 128), &tr1, &bars[bRFull], rx + c * 64, r0);
+            tma_load_2d(smem + L::kR + L::kRBytes + c * (kRes * 128), &tr2, &bars[bRFull],
+                        rx + c * 64, r0);
+          }
+        }
+        r_armed = r_round;
+        ++r_round;
+      }
+      if (!sy.warp(bC1Empty + cst, (cround & 1) ^ 1)) return false;
+      if (lane == 0) {
+        const int cx = (Mode == kModeDQ ? kvh : h) * D;
+        mbar_arrive_expect_tx(&bars[bC1Full + cst], L::kCBytes);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(smem + L::kC1 + cst * L::kCBytes + c * (kSub * 128), &tc1,
+                      &bars[bC1Full + cst], cx + c * 64, c0);
+      }
+      c_armed[cst] = cround;
+      if (++cst == L::NS) {
+        cst = 0;
+        ++cround;
+      }
+      return true;
+    };
+
+    while (ok) {
+      int64_t item = 0;
+      if (lane == 0) item = static_cast<int64_t>(atomicAdd(counter, 1u));
+      item = __shfl_sync(0xffffffffu, item, 0);
+      if (item >= n_items) {
+        ok = push_meta(kStop, kClsF, 0, 0, 0, 0, 0, 0);
+        break;
+      }
+      // dQ: slots in reverse order (the later Q tiles of a causal sample
+      // see the most keys); dK/dV: in order (the first key tiles do)
+      const int64_t u = Mode == kModeDQ ? (p.n_res_slots - 1 - item / n_heads_item)
+                                        : item / n_heads_item;
+      const int hi = static_cast<int>(item % n_heads_item);
+      const int s = slot_sample(p, u, kRes);
+      const int a = clamp_tok(__ldg(p.cu + s), T);
+      const int b = max(a, clamp_tok(__ldg(p.cu + s + 1), T));
+      const int64_t t = u - (static_cast<int64_t>(a) / kRes + s);
+      if (t < 0 || a + t * kRes >= b) continue;  // slot without a tile
+      const int r0 = a + static_cast<int>(t) * kRes;
+      const int r1 = min(r0 + kRes, b);
+      const bool has_mask = p.sri != nullptr;
+
+      if (Mode == kModeDQ) {
+        const int h = hi;
+        const int kvh = h / group;
+        const int mh = p.hm > 1 ? h : 0;
+        const int n_sub = p.causal ? (r1 - 1 - a) / kSub + 1 : (b - a + kSub - 1) / kSub;
+        // key tile k: columns [a + 64k, min(a + 64k + 64, b)), statistics of
+        // the 128-column tile holding it
+        auto cls_of = [&](int k) -> int {
+          if (k >= n_sub) return kClsF;
+          const int c0 = a + k * kSub;
+          const int c1 = min(c0 + kSub, b);
+          int st[8];
+          if (has_mask) load_stats(p, mh, static_cast<int64_t>(a / kStatTile) + s + k / 2, st);
+          return block_class(p, st, r0, r1, c0, c1);
+        };
+        int n_live = 0;
+        for (int base = 0; base < n_sub; base += 32)
+          n_live += __popc(__ballot_sync(0xffffffffu, cls_of(base + lane) != kClsF));
+        if (n_live == 0) {
+          zero_rows<D, Mode, IdxT>(p, r0, r1, h, lane);
+          continue;
+        }
+        int pushed = 0;
+        for (int base = 0; base < n_sub && ok; base += 32) {
+          const int my = cls_of(base + lane);
+          uint32_t live = __ballot_sync(0xffffffffu, my != kClsF);
+          while (live != 0u) {
+            const int l = __ffs(live) - 1;
+            live &= live - 1u;
+            const int cls = __shfl_sync(0xffffffffu, my, l);
+            const int flags = (pushed == 0 ? kFirst : 0) | (pushed == n_live - 1 ? kLast : 0);
+            if (!push_step(flags, cls, a + (base + l) * kSub, r0, b, h, kvh, mh)) {
+              ok = false;
+              break;
+            }
+            ++pushed;
+          }
+        }
+      } else {
+        const int kvh = hi;
+        const int n_qsub = (b - a + kSub - 1) / kSub;
+        const int q_first = p.causal ? (r0 - a) / kSub : 0;
+        const int n_q = n_qsub - q_first;
+        const int64_t sslot = static_cast<int64_t>(a / kStatTile) + s + t;
+        // Q tile q_first + k of q head h: rows [a + 64 (q_first + k), ...)
+        auto cls_of = [&](int h, int k) -> int {
+          if (k >= n_q) return kClsF;
+          const int q0 = a + (q_first + k) * kSub;
+          const int q1 = min(q0 + kSub, b);
+          int st[8];
+          if (has_mask) load_stats(p, p.hm > 1 ? h : 0, sslot, st);
+          return block_class(p, st, q0, q1, r0, r1);
+        };
+        int n_live = 0;
+        for (int h = kvh * group; h < (kvh + 1) * group; ++h)
+          for (int base = 0; base < n_q; base += 32)
+            n_live += __popc(__ballot_sync(0xffffffffu, cls_of(h, base + lane) != kClsF));
+        if (n_live == 0) {
+          zero_rows<D, Mode, IdxT>(p, r0, r1, kvh, lane);
+          continue;
+        }
+        int pushed = 0;
+        for (int h = kvh * group; h < (kvh + 1) * group && ok; ++h) {
+          const int mh = p.hm > 1 ? h : 0;
+          for (int base = 0; base < n_q && ok; base += 32) {
+            const int my = cls_of(h, base + lane);
+            uint32_t live = __ballot_sync(0xffffffffu, my != kClsF);
+            while (live != 0u) {
+              const int l = __ffs(live) - 1;
+              live &= live - 1u;
+              const int cls = __shfl_sync(0xffffffffu, my, l);
+              const int flags = (pushed == 0 ? kFirst : 0) | (pushed == n_live - 1 ? kLast : 0);
+              if (!push_step(flags, cls, a + (q_first + base + l) * kSub, r0, b, h, kvh, mh)) {
+                ok = false;
+                break;
+              }
+              ++pushed;
+            }
+          }
+        }
+      }
+    }
+    if (!ok) {
+      // let every TMA load this warp issued land before the CTA exits
+      for (int st = 0; st < L::NS; ++st)
+        if (c_armed[st] != 0xffffffffu)
+          mbar_wait_bounded(&bars[bC1Full + st], c_armed[st] & 1, 100000000ull, nullptr);
+      if (r_armed != 0xffffffffu)
+        mbar_wait_bounded(&bars[bRFull], r_armed & 1, 100000000ull, nullptr);
+    }
+    bwd_teardown<D>(tmem_slot, warp);
+    return;
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ C2 producer
+    if (lane == 0) {
+      uint32_t cst = 0, cround = 0, mslot = 0, mround = 0;
+      uint32_t c_armed[kMaxStages];
+      for (int i = 0; i < kMaxStages; ++i) c_armed[i] = 0xffffffffu;
+      bool ok = true;
+      for (;;) {
+        if (!sy.lone(bMFull + mslot, mround & 1)) { ok = false; break; }
+        const int flags = *reinterpret_cast<volatile int*>(&meta[mslot].flags);
+        const int c0 = *reinterpret_cast<volatile int*>(&meta[mslot].c0);
+        const int h = *reinterpret_cast<volatile int*>(&meta[mslot].h);
+        const int kvh = *reinterpret_cast<volatile int*>(&meta[mslot].kvh);
+        mbar_arrive(&bars[bMEmpty + mslot]);
+        if (++mslot == kBwdMeta) {
+          mslot = 0;
+          ++mround;
+        }
+        if (flags & kStop) break;
+        if (!sy.lone(bC2Empty + cst, (cround & 1) ^ 1)) { ok = false; break; }
+        const int cx = (Mode == kModeDQ ? kvh : h) * D;
+        mbar_arrive_expect_tx(&bars[bC2Full + cst], L::kCBytes);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(smem + L::kC2 + cst * L::kCBytes + c * (kSub * 128), &tc2,
+                      &bars[bC2Full + cst], cx + c * 64, c0);
+        c_armed[cst] = cround;
+        if (++cst == L::NS) {
+          cst = 0;
+          ++cround;
+        }
+      }
+      if (!ok) {
+        for (int st = 0; st < L::NS; ++st)
+          if (c_armed[st] != 0xffffffffu)
+            mbar_wait_bounded(&bars[bC2Full + st], c_armed[st] & 1, 100000000ull, nullptr);
+      }
+    }
+    bwd_teardown<D>(tmem_slot, warp);
+    return;
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdescXY = idesc_bf16_f32(kRes, kSub, false);
+    constexpr uint32_t kIdescAcc = idesc_bf16_f32(kRes, D, true);
+    const uint32_t r_addr = smem_u32(smem + L::kR);
+    const uint32_t c1_addr = smem_u32(smem + L::kC1);
+    const uint32_t c2_addr = smem_u32(smem + L::kC2);
+    // K-major operands of X / Y; MN-major streamed operands of the
+    // accumulating MMAs (N = D across the 64-column chunks, K = rows)
+    const uint64_t r1_desc = sdesc_sw128(r_addr, 16, 1024);
+    const uint64_t r2_desc = sdesc_sw128(r_addr + L::kRBytes, 16, 1024);
+    const uint64_t c1_desc = sdesc_sw128(c1_addr, 16, 1024);
+    const uint64_t c2_desc = sdesc_sw128(c2_addr, 16, 1024);
+    const uint64_t c1_mn = sdesc_sw128(c1_addr, kSub * 128, 1024);
+    const uint64_t c2_mn = sdesc_sw128(c2_addr, kSub * 128, 1024);
+    constexpr int RC = (kRes * 128) >> 4;  // next 64-column chunk of a resident tile
+    constexpr int CC = (kSub * 128) >> 4;  // next 64-column chunk of a streamed tile
+    constexpr int KS = (16 * 128) >> 4;    // 16 streamed rows (one K step)
+    uint32_t mslot = 0, mround = 0;
+    uint32_t ss_st = 0, ss_round = 0, ts_st = 0;
+    uint32_t r_round = 0, acc_round = 0;
+    bool acc_pending = false;
+    uint32_t n_ss = 0, n_ts = 0;
+    uint32_t rec = 0;  // 4-bit flags of the (at most two) steps with X/Y issued, not yet accumulated
+    bool stopped = false, ok = true;
+
+    auto issue_xy = [&](uint32_t xb, uint32_t st) {
+      const uint64_t cd1 = c1_desc + static_cast<uint64_t>(st * (L::kCBytes >> 4));
+      const uint64_t cd2 = c2_desc + static_cast<uint64_t>(st * (L::kCBytes >> 4));
+      if constexpr (D == 128) {
+        umma_ss_group8<2, 2, 4, 4, 6, 6, RC, CC, RC + 2, CC + 2, RC + 4, CC + 4, RC + 6, CC + 6>(
+            tmem_base + L::x_col(xb), r1_desc, cd1, kIdescXY, 0u);
+        umma_ss_group8<2, 2, 4, 4, 6, 6, RC, CC, RC + 2, CC + 2, RC + 4, CC + 4, RC + 6, CC + 6>(
+            tmem_base + L::y_col(xb), r2_desc, cd2, kIdescXY, 0u);
+      } else {
+        umma_ss_group4<2, 2, 4, 4, 6, 6>(tmem_base + L::x_col(xb), r1_desc, cd1, kIdescXY, 0u);
+        umma_ss_group4<2, 2, 4, 4, 6, 6>(tmem_base + L::y_col(xb), r2_desc, cd2, kIdescXY, 0u);
+      }
+    };
+    auto issue_acc = [&](uint32_t xb, uint32_t st, bool first) {
+      const uint64_t m1 = c1_mn + static_cast<uint64_t>(st * (L::kCBytes >> 4));
+      const uint64_t m2 = c2_mn + static_cast<uint64_t>(st * (L::kCBytes >> 4));
+      const uint32_t acc = first ? 0u : 1u;
+      if (Mode == kModeDQ) {
+        // dQ += dS K
+        umma_ts_group4<KS>(tmem_base + L::kAcc0, tmem_base + L::y_col(xb), m1, kIdescAcc, acc);
+      } else {
+        // dV += P^T dO, dK += dS^T Q
+        umma_ts_group4<KS>(tmem_base + L::kAcc0, tmem_base + L::x_col(xb), m2, kIdescAcc, acc);
+        umma_ts_group4<KS>(tmem_base + L::kAcc1, tmem_base + L::y_col(xb), m1, kIdescAcc, acc);
+      }
+    };
+
+    while (ok) {
+      // X / Y of up to two steps ahead of the accumulating MMAs
+      while (!stopped && n_ss < n_ts + 2) {
+        if (!sy.warp(bMFull + mslot, mround & 1)) { ok = false; break; }
+        const int flags = *reinterpret_cast<volatile int*>(&meta[mslot].flags);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[bMEmpty + mslot]);
+        if (++mslot == kBwdMeta) {
+          mslot = 0;
+          ++mround;
+        }
+        if (flags & kStop) {
+          stopped = true;
+          break;
+        }
+        if (flags & kFirst) {
+          if (!sy.warp(bRFull, r_round & 1)) { ok = false; break; }
+          ++r_round;
+        }
+        if (!sy.warp(bC1Full + ss_st, ss_round & 1)) { ok = false; break; }
+        if (!sy.warp(bC2Full + ss_st, ss_round & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t xb = n_ss & 1u;
+        issue_xy(xb, ss_st);
+        umma_commit_elect(&bars[bSFull + xb]);
+        if (flags & kLast) umma_commit_elect(&bars[bREmpty]);
+        rec = (rec & ~(0xFu << (xb * 4))) | (static_cast<uint32_t>(flags & 0xF) << (xb * 4));
+        ++n_ss;
+        if (++ss_st == L::NS) {
+          ss_st = 0;
+          ++ss_round;
+        }
+      }
+      if (!ok || n_ts == n_ss) break;
+      const uint32_t xb = n_ts & 1u;
+      const int flags = static_cast<int>((rec >> (xb * 4)) & 0xFu);
+      const bool first = (flags & kFirst) != 0;
+      if (!sy.warp(bPFull + xb, (n_ts >> 1) & 1u)) { ok = false; break; }
+      if (first && acc_pending) {
+        if (!sy.warp(bAccEmpty, acc_round & 1)) { ok = false; break; }
+        ++acc_round;
+        acc_pending = false;
+      }
+      tc_fence_after();
+      issue_acc(xb, ts_st, first);
+      umma_commit_elect(&bars[bC1Empty + ts_st]);
+      umma_commit_elect(&bars[bC2Empty + ts_st]);
+      if (flags & kLast) {
+        umma_commit_elect(&bars[bAccFull]);
+        acc_pending = true;
+      }
+      ++n_ts;
+      if (++ts_st == L::NS) ts_st = 0;
+    }
+    // all issued MMAs complete before TMEM is released
+    umma_commit_elect(&bars[bDrain]);
+    mbar_wait_bounded(&bars[bDrain], 0, 100000000ull, nullptr);
+    bwd_teardown<D>(tmem_slot, warp);
+    return;
+  } else {
+    bwd_teardown<D>(tmem_slot, warp);  // idle warp
+  }
+}
+
+// Warps 4..7: P, dS and the epilogue.  Thread = TMEM lane = resident row.
+template <int D, int Mode, typename IdxT>
+__device__ __forceinline__ void bwd_elementwise_role(const AttnBwdParams& p) {
+  using L = BwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
+  const BwdMeta* meta = reinterpret_cast<const BwdMeta*>(smem + L::kMeta);
+  const uint8_t* slots = smem + L::kSlots;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int T = static_cast<int>(p.T);
+  const Sync sy{bars, abort_flag, p.timeout_ns, &p.ws->error_word, lane};
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int row = (warp & 3) * 32 + lane;
+  const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const bool causal = p.causal != 0;
+  const uint64_t c2 = pack_f32x2(p.scale_log2, p.scale_log2);
+  uint32_t mslot = 0, mround = 0, n_steps = 0, acc_cnt = 0;
+  // dQ: -lse*log2(e) and -delta of this row; dK/dV: intervals of this key
+  float nl_row = -CUDART_INF_F, nd_row = 0.f;
+  int lts = 0, lte = 0, uts = 0, ute = 0, cur_mh = -1;
+
+  for (;;) {
+    if (!sy.warp(bMFull + mslot, mround & 1)) break;
+    const int4 ma = *reinterpret_cast<const int4*>(meta + mslot);      // flags, cls, c0, r0
+    const int4 mb = *(reinterpret_cast<const int4*>(meta + mslot) + 1);  // b, h, kvh, mh
+    const int flags = ma.x;
+    if (flags & kStop) break;
+    const int cls = ma.y, c0 = ma.z, r0 = ma.w;
+    const int b = mb.x, h = mb.y, kvh = mb.z, mh = mb.w;
+    const int r = r0 + row;  // resident row of this thread
+    const uint32_t cur_slot = mslot;
+    if (++mslot == kBwdMeta) {
+      mslot = 0;
+      ++mround;
+    }
+    // element mask of the 64 streamed columns (bit set = masked)
+    uint32_t mbits[2] = {0u, 0u};
+    if (Mode == kModeDQ) {
+      if (flags & kFirst) {
+        nl_row = -CUDART_INF_F;
+        nd_row = 0.f;
+        if (r < T) {
+          const IdxT o = static_cast<IdxT>(h) * static_cast<IdxT>(p.T) + static_cast<IdxT>(r);
+          nl_row = __ldg(p.nlse2 + o);
+          nd_row = __ldg(p.ndelta + o);
+        }
+      }
+      // columns = keys c0 + jj; from `valid` on they are outside the sample
+      const int valid = min(kSub, b - c0);
+      if (cls == kClsPC) {
+#pragma unroll
+        for (int w = 0; w < 2; ++w)
+          mbits[w] = range_bits(r - c0 + 1, kSub, w) | range_bits(valid, kSub, w);
+      } else if (cls == kClsP) {
+        const int* cl = reinterpret_cast<const int*>(slots + cur_slot * kSlotBytes);
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          uint32_t bits = 0;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const int jj = w * 32 + i;
+            const int4 a4 = *reinterpret_cast<const int4*>(cl + jj);
+            const int4 e4 = *reinterpret_cast<const int4*>(cl + kSub + jj);
+            const int4 ua4 = *reinterpret_cast<const int4*>(cl + 2 * kSub + jj);
+            const int4 ue4 = *reinterpret_cast<const int4*>(cl + 3 * kSub + jj);
+            const int av[4] = {a4.x, a4.y, a4.z, a4.w};
+            const int ev[4] = {e4.x, e4.y, e4.z, e4.w};
+            const int uav[4] = {ua4.x, ua4.y, ua4.z, ua4.w};
+            const int uev[4] = {ue4.x, ue4.y, ue4.z, ue4.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const bool lower = r >= c0 + jj + q;
+              const bool in_lt = (av[q] <= r) & (r < ev[q]);
+              const bool in_ut = causal | ((uav[q] <= r) & (r < uev[q]));
+              const bool m = (jj + q >= valid) | (lower ? in_lt : in_ut);
+              bits |= static_cast<uint32_t>(m) << (i + q);
+            }
+          }
+          mbits[w] = bits;
+        }
+      } else {
+#pragma unroll
+        for (int w = 0; w < 2; ++w) mbits[w] = range_bits(valid, kSub, w);
+      }
+    } else {
+      // columns = queries c0 + jj; rows outside the sample already carry
+      // -lse*log2(e) = -inf
+      if (flags & kFirst) cur_mh = -1;  // new key rows
+      if (cls == kClsP && mh != cur_mh) {
+        cur_mh = mh;
+        lts = lte = uts = ute = 0;
+        if (r < T) {
+          const int32_t* src = p.sri + static_cast<int64_t>(mh) * 4 * p.T + r;
+          lts = __ldg(src);
+          lte = __ldg(src + p.T);
+          uts = __ldg(src + 2 * p.T);
+          ute = __ldg(src + 3 * p.T);
+        }
+      }
+      if (cls == kClsPC) {
+        // query rows above the key (i < j) are masked
+#pragma unroll
+        for (int w = 0; w < 2; ++w) mbits[w] = range_bits(0, r - c0, w);
+      } else if (cls == kClsP) {
+        // i >= j: masked iff LTS <= i < LTE; i < j: iff causal or UTS <= i < UTE
+        const int lo0 = max(lts, r) - c0, lo1 = lte - c0;
+        const int up0 = causal ? 0 : uts - c0;
+        const int up1 = (causal ? r : min(ute, r)) - c0;
+#pragma unroll
+        for (int w = 0; w < 2; ++w) mbits[w] = range_bits(lo0, lo1, w) | range_bits(up0, up1, w);
+      }
+    }
+
+    const uint32_t xb = n_steps & 1u;
+    if (!sy.warp(bSFull + xb, (n_steps >> 1) & 1u)) break;
+    tc_fence_after();
+    const uint32_t x_t = tmem_base + lane_addr + L::x_col(xb);
+    const uint32_t y_t = tmem_base + lane_addr + L::y_col(xb);
+    const float* nl_col = reinterpret_cast<const float*>(slots + cur_slot * kSlotBytes);
+    const float* nd_col = nl_col + kSub;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t xr[32], yr[32];
+      tmem_ld32(x_t + half * 32, xr);
+      tmem_ld32(y_t + half * 32, yr);
+      const uint32_t mw = mbits[half];
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if ((mw >> j) & 1u) xr[j] = __float_as_uint(-CUDART_INF_F);
+      uint32_t pk[16], dk[16];
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        uint64_t nl2, nd2;
+        if (Mode == kModeDQ) {
+          nl2 = pack_f32x2(nl_row, nl_row);
+          nd2 = pack_f32x2(nd_row, nd_row);
+        } else {
+          const float2 a2 = *reinterpret_cast<const float2*>(nl_col + half * 32 + j);
+          const float2 d2 = *reinterpret_cast<const float2*>(nd_col + half * 32 + j);
+          nl2 = pack_f32x2(a2.x, a2.y);
+          nd2 = pack_f32x2(d2.x, d2.y);
+        }
+        bwd_pair(xr[j], xr[j + 1], yr[j], yr[j + 1], c2, nl2, nd2, pk[j >> 1], dk[j >> 1]);
+      }
+      if (Mode == kModeDKV) tmem_st16(x_t + half * 16, pk);
+      tmem_st16(y_t + half * 16, dk);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(&bars[bPFull + xb]);
+    // metadata and per-step data of this step are no longer needed
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[bMEmpty + cur_slot]);
+
+    if (flags & kLast) {
+      if (!sy.warp(bAccFull, acc_cnt & 1u)) break;
+      ++acc_cnt;
+      tc_fence_after();
+      const bool store = r < b;
+      const int heads = Mode == kModeDQ ? p.hq : p.hkv;
+      const int hh = Mode == kModeDQ ? h : kvh;
+      const IdxT off = (static_cast<IdxT>(store ? r : 0) * heads + hh) * static_cast<IdxT>(D);
+      const int n_acc = Mode == kModeDQ ? 1 : 2;
+#pragma unroll
+      for (int which = 0; which < n_acc; ++which) {
+        // dQ (scaled) / dV (unscaled) from kAcc0, dK (scaled) from kAcc1
+        const float f = (Mode == kModeDKV && which == 0) ? 1.f : p.scale;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(
+                                 Mode == kModeDQ ? p.dq : (which == 0 ? p.dv : p.dk)) +
+                             off;
+        const uint32_t acc_t = tmem_base + lane_addr + (which == 0 ? L::kAcc0 : L::kAcc1);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(acc_t + c * 32, rr);
+          if (store) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              d4[u] = make_uint4(pack_bf16x2(__uint_as_float(rr[8 * u + 0]) * f,
+                                             __uint_as_float(rr[8 * u + 1]) * f),
+                                 pack_bf16x2(__uint_as_float(rr[8 * u + 2]) * f,
+                                             __uint_as_float(rr[8 * u + 3]) * f),
+                                 pack_bf16x2(__uint_as_float(rr[8 * u + 4]) * f,
+                                             __uint_as_float(rr[8 * u + 5]) * f),
+                                 pack_bf16x2(__uint_as_float(rr[8 * u + 6]) * f,
+                                             __uint_as_float(rr[8 * u + 7]) * f));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars[bAccEmpty]);
+    }
+    ++n_steps;
+  }
+  bwd_teardown<D>(tmem_slot, warp);
+}
+
+template <int D, int Mode, typename IdxT>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_kernel(const AttnBwdParams p, const __grid_constant__ CUtensorMap tr1,
+                    const __grid_constant__ CUtensorMap tr2,
+                    const __grid_constant__ CUtensorMap tc1,
+                    const __grid_constant__ CUtensorMap tc2) {
+  if ((threadIdx.x >> 5) < 4)
+    bwd_producer_roles<D, Mode, IdxT>(p, tr1, tr2, tc1, tc2);
+  else
+    bwd_elementwise_role<D, Mode, IdxT>(p);
+}
+
+template <int D, int Mode, typename IdxT>
+cudaError_t launch_mode(const AttnBwdParams& p, const CUtensorMap& tr1, const CUtensorMap& tr2,
+                        const CUtensorMap& tc1, const CUtensorMap& tc2, int num_sms,
+                        cudaStream_t stream) {
+  using L = BwdLayout<D>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static unsigned long long configured = 0ull;  // one bit per device
+  if (dev >= 64 || !((configured >> dev) & 1ull)) {
+    e = cudaFuncSetAttribute(attn_bwd_kernel<D, Mode, IdxT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) configured |= 1ull << dev;
+  }
+  const int64_t items = p.n_res_slots * (Mode == kModeDQ ? p.hq : p.hkv);
+  const int grid = static_cast<int>(items < num_sms ? items : num_sms);
+  attn_bwd_kernel<D, Mode, IdxT><<<grid, kBwdThreads, L::kBytes, stream>>>(p, tr1, tr2, tc1, tc2);
+  return cudaGetLastError();
+}
+
+template <int D, typename IdxT>
+cudaError_t launch_all(const AttnBwdParams& p, const BwdMaps& m, int num_sms,
+                       cudaStream_t stream) {
+  const int64_t rows = p.T * p.hq;
+  const int64_t blocks = (rows * (D / 8) + 255) / 256;
+  bwd_prep_kernel<D, IdxT><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_mode<D, kModeDKV, IdxT>(p, m.k128, m.v128, m.q64, m.do64, num_sms, stream);
+  if (e != cudaSuccess) return e;
+  return launch_mode<D, kModeDQ, IdxT>(p, m.q128, m.do128, m.k64, m.v64, num_sms, stream);
+}
+
+}  // namespace
+
+size_t attn_bwd_workspace_bytes(int64_t T, int n_heads_q) {
+  const size_t bytes = sizeof(AttnWorkspaceHeader) + 2 * static_cast<size_t>(T) * n_heads_q * 4;
+  return (bytes + 255) & ~static_cast<size_t>(255);
+}
+
+cudaError_t launch_attn_bwd(const AttnBwdParams& p, const BwdMaps& maps, bool use_int64,
+                            int num_sms, cudaStream_t stream) {
+  if (p.head_dim == 128)
+    return use_int64 ? launch_all<128, int64_t>(p, maps, num_sms, stream)
+                     : launch_all<128, int32_t>(p, maps, num_sms, stream);
+  return use_int64 ? launch_all<64, int64_t>(p, maps, num_sms, stream)
+                   : launch_all<64, int32_t>(p, maps, num_sms, stream);
+}
+
+}  // namespace fm

@@ -258,6 +258,101 @@ fm_status fm_attn_fwd_varlen(const void* q, const void* k, const void* v, int64_
   return from_cuda(fm::launch_attn_fwd(p, tq, tk, tv, use64, num_sms, s));
 }
 
+size_t fm_attn_bwd_workspace_size(int64_t total_tokens, int n_heads_q) {
+  if (total_tokens < 0 || n_heads_q < 1) return 0;
+  return fm::attn_bwd_workspace_bytes(total_tokens, n_heads_q);
+}
+
+fm_status fm_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* out,
+                             const void* dout, const float* lse, int64_t total_tokens,
+                             int n_heads_q, int n_heads_kv, int head_dim,
+                             const int32_t* cu_seqlens, int n_seqs,
+                             const int32_t* startend_row_indices, int n_mask_heads,
+                             const int32_t* block_minmax, int causal, float softmax_scale,
+                             void* dq, void* dk, void* dv, void* workspace,
+                             size_t workspace_bytes, uint32_t flags, void* stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || dout == nullptr ||
+      lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
+      cu_seqlens == nullptr || workspace == nullptr)
+    return FM_ERR_INVALID_ARG;
+  if (total_tokens < 0 || total_tokens > INT32_MAX - 256 || n_seqs < 1) return FM_ERR_INVALID_ARG;
+  if (n_heads_q < 1 || n_heads_kv < 1 || n_heads_q % n_heads_kv != 0) return FM_ERR_INVALID_ARG;
+  if (flags & ~FM_FLAG_FORCE_INT64) return FM_ERR_INVALID_ARG;
+  if (startend_row_indices != nullptr) {
+    if (n_mask_heads != 1 && n_mask_heads != n_heads_q) return FM_ERR_INVALID_ARG;
+    if (block_minmax == nullptr) return FM_ERR_INVALID_ARG;
+  } else {
+    if (block_minmax != nullptr) return FM_ERR_INVALID_ARG;
+    n_mask_heads = 0;
+  }
+  if (!(softmax_scale >= 0.0f) || !std::isfinite(softmax_scale)) return FM_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return FM_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4) || !aligned(workspace, 256))
+    return FM_ERR_ALIGNMENT;
+  if (workspace_bytes < fm::attn_bwd_workspace_bytes(total_tokens, n_heads_q))
+    return FM_ERR_WORKSPACE;
+  const int64_t n_slots = total_tokens / 128 + n_seqs;
+  if (n_slots * n_heads_q >= (int64_t(1) << 31)) return FM_ERR_UNSUPPORTED;
+  if (total_tokens == 0) return FM_OK;
+  int num_sms = 0;
+  fm_status st = device_info(&num_sms);
+  if (st != FM_OK) return st;
+
+  fm::BwdMaps m;
+  const uint64_t T = static_cast<uint64_t>(total_tokens);
+  const uint64_t qc = static_cast<uint64_t>(n_heads_q) * head_dim;
+  const uint64_t kc = static_cast<uint64_t>(n_heads_kv) * head_dim;
+  if (!make_map(&m.q128, q, qc, T, 128) || !make_map(&m.do128, dout, qc, T, 128) ||
+      !make_map(&m.k128, k, kc, T, 128) || !make_map(&m.v128, v, kc, T, 128) ||
+      !make_map(&m.q64, q, qc, T, 64) || !make_map(&m.do64, dout, qc, T, 64) ||
+      !make_map(&m.k64, k, kc, T, 64) || !make_map(&m.v64, v, kc, T, 64))
+    return FM_ERR_CUDA;
+
+  fm::AttnBwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.dout = dout;
+  p.lse = lse;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.cu = cu_seqlens;
+  p.sri = startend_row_indices;
+  p.minmax = block_minmax;
+  p.ws = reinterpret_cast<fm::AttnWorkspaceHeader*>(ws);
+  p.nlse2 = reinterpret_cast<float*>(ws + sizeof(fm::AttnWorkspaceHeader));
+  p.ndelta = p.nlse2 + total_tokens * n_heads_q;
+  p.T = total_tokens;
+  p.n_res_slots = n_slots;
+  p.n_kv_slots = fm_num_kv_tiles_bound(total_tokens, n_seqs, 128);
+  p.n_seqs = n_seqs;
+  p.hq = n_heads_q;
+  p.hkv = n_heads_kv;
+  p.hm = n_mask_heads;
+  p.head_dim = head_dim;
+  p.causal = causal != 0;
+  const double scale = softmax_scale > 0.0f ? softmax_scale : 1.0 / std::sqrt(double(head_dim));
+  p.scale = static_cast<float>(scale);
+  p.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
+  p.timeout_ns = 1000000000ull;
+
+  const int64_t lim = int64_t(1) << 31;
+  const bool use64 = (flags & FM_FLAG_FORCE_INT64) != 0 ||
+                     total_tokens * n_heads_q * head_dim >= lim ||
+                     total_tokens * n_heads_kv * head_dim >= lim;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, sizeof(fm::AttnWorkspaceHeader), s) != cudaSuccess)
+    return FM_ERR_CUDA;
+  return from_cuda(fm::launch_attn_bwd(p, m, use64, num_sms, s));
+}
+
 fm_status fm_attn_fwd_num_work_items(const void* workspace, int64_t* host_items, void* stream) {
   if (workspace == nullptr || host_items == nullptr) return FM_ERR_INVALID_ARG;
   const auto* hdr = static_cast<const fm::AttnWorkspaceHeader*>(workspace);

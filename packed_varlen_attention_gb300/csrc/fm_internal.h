@@ -34,7 +34,8 @@ struct AttnWorkspaceHeader {
   int32_t n_items;        // work items: (pair of Q tiles) x Hq
   int32_t error_word;     // FM_DEVERR_* bits
   int32_t n_tile_items;   // n_qtiles * Hq
-  int32_t pad[59];
+  uint32_t work_counter_kv;  // backward: next key/value work item (atomic)
+  int32_t pad[58];
 };
 static_assert(sizeof(AttnWorkspaceHeader) == 256, "header is 256 bytes");
 
@@ -74,5 +75,46 @@ cudaError_t launch_attn_fwd(const AttnParams& p, const CUtensorMap& tq, const CU
                             cudaStream_t stream);
 
 cudaError_t launch_bounded_wait_probe(int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
+
+// Attention backward: 128-row resident tiles, 64-row streamed tiles, block
+// statistics of 128-column key tiles.
+struct AttnBwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* out;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  const int32_t* cu;
+  const int32_t* sri;
+  const int32_t* minmax;
+  AttnWorkspaceHeader* ws;
+  float* nlse2;   // [Hq][T]: -lse * log2(e), -inf for rows with no unmasked key
+  float* ndelta;  // [Hq][T]: -(dout . out) per row
+  int64_t T;
+  int64_t n_res_slots;  // floor(T / 128) + n_seqs: 128-row tile slots
+  int64_t n_kv_slots;   // slots of the block statistics (same formula)
+  int n_seqs;
+  int hq, hkv, hm;
+  int head_dim;
+  int causal;
+  float scale;
+  float scale_log2;
+  uint64_t timeout_ns;
+};
+
+// Tensor maps of the backward pass: 128-row and 64-row boxes of q, k, v, dout.
+struct BwdMaps {
+  CUtensorMap q128, do128, k128, v128;
+  CUtensorMap q64, do64, k64, v64;
+};
+
+size_t attn_bwd_workspace_bytes(int64_t T, int n_heads_q);
+
+cudaError_t launch_attn_bwd(const AttnBwdParams& p, const BwdMaps& maps, bool use_int64,
+                            int num_sms, cudaStream_t stream);
 
 }  // namespace fm

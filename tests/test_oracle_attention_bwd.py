@@ -103,3 +103,23 @@ def test_row_delta_is_rowsum_of_p_times_dp():
             js = np.arange(s, i + 1)
             p = np.exp((q[i, h] @ k[js, 0].T) / np.sqrt(8) - lse[h, i])
             assert abs(delta[h, i] - (p * (v[js, 0] @ do[i, h])).sum()) < 1e-12
+
+
+def test_magnitude_sums_bound_the_gradients():
+    # |sum of terms| <= sum of |terms|; with dout >= 0 the dv sum has no
+    # cancellation and equals its magnitude sum
+    wl = gen.make_custom([9, 14], n_heads_q=4, n_heads_kv=2, head_dim=8, mask="window",
+                         window=5, seed=4, tensors=False)
+    rng = np.random.default_rng(9)
+    T = wl.total_tokens
+    q, do = rng.standard_normal((T, 4, 8)), rng.standard_normal((T, 4, 8))
+    k, v = rng.standard_normal((T, 2, 8)), rng.standard_normal((T, 2, 8))
+    cu, sri = wl.cu_seqlens, wl.startend_row_indices
+    dq, dk, dv, mq, mk, mv = ob.attention_backward(q, k, v, do, cu, sri, True, magnitudes=True)
+    assert np.all(mq >= np.abs(dq) - 1e-12)
+    assert np.all(mk >= np.abs(dk) - 1e-12)
+    assert np.all(mv >= np.abs(dv) - 1e-12)
+    g = ob.attention_backward(q, k, v, np.abs(do), cu, sri, True, magnitudes=True)
+    np.testing.assert_allclose(g[2], g[5], rtol=1e-12)
+    # the gradients themselves do not depend on the option
+    np.testing.assert_array_equal(ob.attention_backward(q, k, v, do, cu, sri, True)[0], dq)
