@@ -234,6 +234,19 @@ class Batch:
         self.h2d_bytes = sum(t.numel() * t.element_size()
                              for t in (self.h_q, self.h_k, self.h_v, self.h_cu, self.h_sri))
         self.d2h_bytes = self.out.numel() * 2 + self.lse.numel() * 4
+        # backward: a seeded output gradient, gradient buffers, block
+        # statistics of 128-column key tiles, workspace
+        rng = np.random.default_rng(4242 + wl.seed)
+        self.dout = dt(gen.f32_to_bf16_bits(
+            rng.standard_normal(wl.q_bits.shape, dtype=np.float32))).to(device)
+        self.dq = torch.empty_like(self.q)
+        self.dk = torch.empty_like(self.k)
+        self.dv = torch.empty_like(self.v)
+        self.mm128 = self.mm if wl.block_n == 128 else torch.empty(
+            (self.sri.shape[0], 8, fm.num_kv_tiles_bound(T, n, 128)), dtype=torch.int32,
+            device=device)
+        self.bws = torch.empty(fm.attn_bwd_workspace_size(T, wl.n_heads_q), dtype=torch.uint8,
+                               device=device)
 
     def restore(self):
         self.q.copy_(self.q0)
@@ -254,6 +267,20 @@ class Batch:
                            class_counts=counts, workspace=self.ws, force_int64=wl.force_int64)
         if events:
             events[3].record()
+
+    def backward(self, fm):
+        """Gradients of the step's attention (q, k after RoPE; out, lse of the step)."""
+        wl = self.wl
+        fm.attn_bwd_varlen(self.q, self.k, self.v, self.out, self.dout, self.lse, self.cu,
+                           self.sri, self.mm128, causal=wl.causal, dq=self.dq, dk=self.dk,
+                           dv=self.dv, workspace=self.bws, force_int64=wl.force_int64)
+
+    def prepare_backward(self, fm):
+        """One forward step so that out / lse / rotated q, k exist; 128-column statistics."""
+        self.restore()
+        self.step(fm)
+        if self.mm128 is not self.mm:
+            fm.mask_block_minmax(self.sri, self.cu, 128, out=self.mm128)
 
     def step_e2e(self, fm):
         """Same step through host buffers: H2D inputs, compute, D2H result."""
@@ -286,6 +313,34 @@ def time_config(fm, torch, batch, steps, warmup, flush, peaks):
     return {"rope_ms": float(np.mean(rope)), "minmax_ms": float(np.mean(mm)),
             "attn_ms": float(np.mean(attn)), "step_ms": float(np.mean(tot)),
             "step_ms_sum": float(np.sum(tot))}
+
+
+def time_backward(fm, torch, batch, steps, warmup, flush):
+    """Mean device time (ms) of one fm_attn_bwd_varlen call (prep + dK/dV +
+    dQ kernels), L2 flushed before each call."""
+    batch.prepare_backward(fm)
+    for _ in range(warmup):
+        batch.backward(fm)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        evs[i][0].record()
+        batch.backward(fm)
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    if fm.get_device_error(batch.bws) != 0:
+        raise RuntimeError("attention backward reported a device error")
+    return float(np.mean([a.elapsed_time(b) for a, b in evs]))
+
+
+def backward_entry(fl, ms, peaks):
+    """Backward accounting: 10 * head_dim FLOPs per unmasked pair and q head
+    (the five products S, dP, dV, dK, dQ), i.e. 2.5 x the forward count."""
+    tf = 2.5 * fl / (ms * 1e-3) / 1e12
+    return {"ms": ms, "effective_tflops": tf, "frac_of_measured_bf16_peak": tf / peaks["bf16_tflops"],
+            "effective_tflop_per_call": 2.5 * fl / 1e12}
 
 
 def run_ours(args):
@@ -325,6 +380,8 @@ def run_ours(args):
             "block_counts_fpu": counts.cpu().tolist(),
             "tokens": wl.total_tokens,
         }
+        per_config[gen.CONFIG_NAMES[cfg]]["backward"] = backward_entry(
+            fl, time_backward(fm, torch, b, max(5, min(args.steps, 20)), 3, flush), peaks)
         del b
         torch.cuda.empty_cache()
 
@@ -372,6 +429,8 @@ def run_ours(args):
         e2e_stop.record()
         e2e_stop.synchronize()
         e2e_ms.append(e2e_start.elapsed_time(e2e_stop))
+    # backward of the same batch (outside the step's timed region)
+    bwd_ms = time_backward(fm, torch, b, args.steps, max(3, args.warmup), flush)
     clocks = sampler.stop()
 
     step_ms = [e[0].elapsed_time(e[3]) for e in evs]
@@ -404,6 +463,7 @@ def run_ours(args):
         "minmax_us": mm_ms * 1e3, "attn_ms": attn_ms, "rope_ms": rope_ms,
         "step_ms": float(np.mean(step_ms)), "effective_tflop_per_step": fl / 1e12,
         "block_counts_fpu": counts.cpu().tolist(), "tokens": wl.total_tokens,
+        "backward": backward_entry(fl, bwd_ms, peaks),
     }
     line = {
         "metric": METRIC,
@@ -438,6 +498,11 @@ def run_ours(args):
             "traffic": measured_traffic(),
             "traffic_unit": "bytes per launch (ncu dram read + write, headline workload)",
         },
+        "backward": dict(backward_entry(fl, bwd_ms, peaks), **{
+            "call": "attn_bwd_varlen (prep + dK/dV kernel + dQ kernel), same batch, dout seeded",
+            "bound": "tensor", "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "peak_source": f"{peak_src} bf16 burst",
+            "launches_per_call": 3}),
         "rope": {"bound": "hbm", "achieved": rope_gbs, "unit": "GB/s",
                  "peak": peaks["hbm_gbs"], "frac": rope_gbs / peaks["hbm_gbs"],
                  "frac_of_8tbs": rope_gbs / 8000.0, "bytes": rb},

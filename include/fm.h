@@ -297,6 +297,15 @@ FM_API fm_status fm_attn_fwd_num_work_items(const void* workspace, int64_t* host
 FM_API fm_status fm_get_device_error(const void* workspace, int32_t* host_err, void* stream);
 
 /*
+ * fm_get_device_timeout_info -- synchronises `stream` and copies four int32
+ * describing the first pipeline wait that ran out in the last call that used
+ * `workspace`: {1 if one did (else 0), barrier index, phase parity,
+ * block << 8 | warp}.  Barrier indices are internal to each kernel; this is
+ * a diagnostic for bug reports, not an interface to act on.
+ */
+FM_API fm_status fm_get_device_timeout_info(const void* workspace, int32_t* host_info, void* stream);
+
+/*
  * fm_debug_bounded_wait -- runs the pipeline's bounded mbarrier wait once on
  * a barrier that nothing ever arrives at, with a limit of timeout_ns, and
  * writes the resulting status (FM_ERR_TIMEOUT when the limit expired) to

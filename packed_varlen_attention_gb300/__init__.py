@@ -34,6 +34,7 @@ __all__ = [
     "attn_bwd_workspace_size",
     "attn_bwd_varlen",
     "get_device_error",
+    "get_device_timeout_info",
     "debug_bounded_wait",
     "status_string",
     "version",
@@ -76,6 +77,7 @@ _SIGNATURES = {
                                     ctypes.c_float, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t,
                                     _c_u32, _c_vp]),
     "fm_get_device_error": (_c_int, [_c_vp, ctypes.POINTER(ctypes.c_int32), _c_vp]),
+    "fm_get_device_timeout_info": (_c_int, [_c_vp, ctypes.POINTER(ctypes.c_int32), _c_vp]),
     "fm_debug_bounded_wait": (_c_int, [_c_vp, ctypes.c_uint64, _c_vp]),
     "fm_status_string": (ctypes.c_char_p, [_c_int]),
     "fm_version": (_c_int, []),
@@ -336,6 +338,14 @@ def get_device_error(workspace: torch.Tensor, stream=None) -> int:
     _check("fm_get_device_error",
            _lib().fm_get_device_error(_ptr(workspace), ctypes.byref(e), _stream(stream)))
     return int(e.value)
+
+
+def get_device_timeout_info(workspace: torch.Tensor, stream=None):
+    """(expired, barrier, parity, block, warp) of the first wait that ran out."""
+    info = (ctypes.c_int32 * 4)()
+    _check("fm_get_device_timeout_info", _lib().fm_get_device_timeout_info(
+        _ptr(workspace), info, _stream(stream)))
+    return (int(info[0]), int(info[1]), int(info[2]), int(info[3]) >> 8, int(info[3]) & 0xFF)
 
 
 def debug_bounded_wait(timeout_ns: int, stream=None) -> int:

@@ -25,22 +25,23 @@
 //   * dQ kernel: a work item is one 128-row Q tile of one q head; it walks
 //     the 64-key tiles that are not fully masked, keeping dQ in TMEM.
 // Both are one persistent kernel template (one CTA per SM pulling items from
-// an atomic counter) with the same warp roles (256 threads):
+// an atomic counter) with the same warp roles (384 threads):
 //   warp 0   producer: block classes of the item's steps, per-step metadata
 //            in an 8-slot ring, TMA loads of the two resident tiles (R1, R2:
 //            K, V or Q, dO; 128 rows) once per item and of the first
 //            streamed tile (C1: Q or K; 64 rows) per step;
 //   warp 2   TMA loads of the second streamed tile (C2: dO or V) per step;
-//   warp 1   MMA issuer (whole warp converged, elect.sync picks the lane):
-//            X = R1 C1^T and Y = R2 C2^T (tcgen05.mma kind::f16, M = 128,
-//            N = 64, fp32 in TMEM, two buffers), then with operand A read
-//            from TMEM: dV += P^T dO and dK += dS^T Q, or dQ += dS K;
-//   warps 4..7  elementwise, one thread per TMEM lane: masks X, forms
+//   warp 1   MMA issuer of X = R1 C1^T and Y = R2 C2^T (tcgen05.mma
+//            kind::f16, M = 128, N = 64, fp32 in TMEM, two buffers);
+//   warp 3   MMA issuer of the accumulating products, operand A read from
+//            TMEM: dV += P^T dO and dK += dS^T Q, or dQ += dS K;
+//   warps 4..11  elementwise, two warpgroups, one thread per TMEM lane,
+//            each warpgroup 32 of the 64 streamed columns: masks X, forms
 //            P = 2^(X * scale * log2 e - lse * log2 e) and
 //            dS = P * (Y - delta), stores them as bf16 into TMEM over X and
 //            Y, and writes the gradients of the item at its end.
-// The X/Y stream runs two steps ahead of the accumulating MMAs, so the
-// elementwise warps work on step t while the tensor cores run step t+1.
+// X / Y of step t+1 run on the tensor cores while the elementwise warps work
+// on step t.
 // Every mbarrier wait is bounded and reports FM_DEVERR_TIMEOUT instead of
 // hanging.
 #include <cuda_bf16.h>
@@ -55,7 +56,7 @@ namespace {
 
 enum : int { kModeDQ = 0, kModeDKV = 1 };
 
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 384;
 constexpr int kRes = 128;       // resident tile rows = TMEM lanes
 constexpr int kSub = 64;        // streamed tile rows
 constexpr int kStatTile = 128;  // key tile of the block statistics
@@ -81,29 +82,41 @@ struct BwdMeta {
 };
 static_assert(sizeof(BwdMeta) == 64, "BwdMeta is 64 bytes");
 
+constexpr int kMaxBufs = 3;  // X / Y buffers: 3 for dQ, 2 for dK/dV (TMEM budget)
+
 enum BwdBar : int {
-  bC1Full = 0,
-  bC1Empty = bC1Full + kMaxStages,
-  bC2Full = bC1Empty + kMaxStages,
-  bC2Empty = bC2Full + kMaxStages,
-  bMFull = bC2Empty + kMaxStages,
-  bMEmpty = bMFull + kBwdMeta,
-  bRFull = bMEmpty + kBwdMeta,  // both resident tiles of an item landed
+  bCFull = 0,                      // [stages] both streamed tiles landed (two producers)
+  bCEmpty = bCFull + kMaxStages,   // [stages] accumulating MMAs of the step done
+  bMFull = bCEmpty + kMaxStages,
+  bRFull = bMFull + kBwdMeta,   // both resident tiles of an item landed
   bREmpty,                      // last X/Y MMAs of an item done
-  bSFull,                       // [2 buffers] X and Y ready
-  bPFull = bSFull + 2,          // [2 buffers] P / dS written (128 arrivals)
-  bAccFull = bPFull + 2,        // last accumulating MMA of an item done
-  bAccEmpty,                    // accumulators read by the epilogue (128 arrivals)
-  bDrain,
-  bNumBars
+  bSFull,                       // [buffers] X and Y ready
+  bPFull = bSFull + kMaxBufs,   // [buffers] P / dS written (one arrival per warp)
+  bAccFull = bPFull + kMaxBufs, // last accumulating MMA of an item done
+  bAccEmpty,                    // accumulators read by the epilogue (one per warp)
+  bTSDone,                      // [buffers] accumulating MMAs of the buffer's step done
+  bDrain = bTSDone + kMaxBufs,  // [2 issuers]
+  bNumBars = bDrain + 2
 };
 
-// arrivals on bMEmpty: the issuer, the C2 producer and the four elementwise warps
-constexpr int kBwdMEmptyCount = 6;
+// A metadata slot needs no release barrier: the producer writes slot u mod 8
+// only after stage (u - 1) mod NS was freed, i.e. after the accumulating MMAs
+// of step u - 1 - NS, which follow every read of steps <= u - 1 - NS (the
+// elementwise warps read a step's slot before its P-full, the C2 producer
+// before its load).  The slot's previous step u - 8 is among them when
+// NS <= 7.
+static_assert(kBwdStages<64> <= kBwdMeta - 1 && kBwdStages<128> <= kBwdMeta - 1,
+              "metadata ring reuse is ordered by the stage ring");
+// arrivals on bPFull and bAccEmpty: one per elementwise warp
+constexpr int kBwdEwWarps = 8;
 
-template <int D>
+template <int D, int Mode>
 struct BwdLayout {
   static constexpr int NS = kBwdStages<D>;
+  // X / Y buffers: the loop X/Y ready -> P/dS -> accumulating MMAs -> buffer
+  // free spans NB steps.  dK/dV keeps two fp32 accumulators (2 D columns) in
+  // TMEM and fits two buffers; dQ keeps one and fits three.
+  static constexpr int NB = Mode == kModeDQ ? 3 : 2;
   static constexpr int kRBytes = kRes * D * 2;
   static constexpr int kCBytes = kSub * D * 2;
   static constexpr int kR = 0;  // R1, then R2
@@ -111,19 +124,25 @@ struct BwdLayout {
   static constexpr int kC2 = kC1 + NS * kCBytes;
   static constexpr int kSlots = kC2 + NS * kCBytes;  // per-step data, kSlotBytes each
   static constexpr int kMeta = kSlots + kBwdMeta * kSlotBytes;
-  static constexpr int kBars = kMeta + kBwdMeta * static_cast<int>(sizeof(BwdMeta));
+  // flags of the step held by each stage (published by the stage's full
+  // barrier) and of the step in each X / Y buffer (published by P-full)
+  static constexpr int kStageFlags = kMeta + kBwdMeta * static_cast<int>(sizeof(BwdMeta));
+  static constexpr int kBufFlags = kStageFlags + kMaxStages * 4;
+  static constexpr int kBars = kBufFlags + 16;
   static constexpr int kTmemSlot = kBars + bNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kEnd = kAbort + 4;
   static constexpr int kBytes = kEnd + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  // TMEM columns: X of buffer b at 64 b (P over its first 32), Y at
-  // 128 + 64 b (dS over its first 32), accumulators at 256 (dQ or dV) and
-  // 256 + D (dK).
+  // TMEM columns: X of buffer b at 64 b (P packed over its columns 0..15
+  // and 32..47), Y at 64 (NB + b) (dS likewise), accumulators from 128 NB:
+  // dQ, or dV then dK.
   __host__ __device__ static constexpr uint32_t x_col(uint32_t b) { return 64u * b; }
-  __host__ __device__ static constexpr uint32_t y_col(uint32_t b) { return 128u + 64u * b; }
-  static constexpr uint32_t kAcc0 = 256;
-  static constexpr uint32_t kAcc1 = 256 + D;
+  __host__ __device__ static constexpr uint32_t y_col(uint32_t b) { return 64u * (NB + b); }
+  static constexpr uint32_t kAcc0 = 128 * NB;
+  static constexpr uint32_t kAcc1 = 128 * NB + D;
+  static_assert(kAcc0 + (Mode == kModeDQ ? D : 2 * D) <= kTmemCols, "TMEM budget");
+  static_assert(NB <= kMaxBufs, "buffer barriers");
   static_assert(NS <= kMaxStages, "stage barriers");
   static_assert(kBytes <= 232448, "shared memory budget");
   static_assert(kSub * 4 * 4 <= kSlotBytes, "slot holds four interval vectors");
@@ -168,6 +187,43 @@ __device__ __forceinline__ void bwd_pair(uint32_t x0, uint32_t x1, uint32_t y0, 
       "cvt.rn.bf16x2.f32 %1, t1, t0;\n\t}"
       : "=r"(pk), "=r"(dsk)
       : "r"(x0), "r"(x1), "r"(y0), "r"(y1), "l"(c2), "l"(nl2), "l"(nd2));
+}
+
+// 32 consecutive columns at each of two TMEM addresses, one wait for both.
+__device__ __forceinline__ void tmem_ld32_pair(uint32_t ta, uint32_t tb, uint32_t (&a)[32],
+                                               uint32_t (&b)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]), "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]), "=r"(b[16]), "=r"(b[17]), "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]), "=r"(b[24]), "=r"(b[25]), "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31])
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+
+// Four accumulating MMAs (K = 16 each) whose A operand comes from TMEM at
+// column offsets 0, 8, 32, 40 (the packed halves the two elementwise
+// warpgroups write) and whose B operand advances by OB per step.
+template <int OB>
+__device__ __forceinline__ void umma_ts_group4_split(uint32_t d_tmem, uint32_t a_tmem,
+                                                     uint64_t b_desc, uint32_t idesc,
+                                                     uint32_t acc0) {
+  asm volatile("{\n\t.reg .pred p, q, e;\n\t.reg .b32 el;\n\t"
+               ".reg .b64 b;\n\t.reg .b32 a;\n\t"
+               "elect.sync el|e, 0xffffffff;\n\t"
+               "setp.ne.b32 p, %4, 0;\n\t"
+               "setp.eq.u32 q, 0, 0;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+               "add.u32 a, %1, 8;\n\tadd.s64 b, %2, %5;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "add.u32 a, %1, 32;\n\tadd.s64 b, %2, %6;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "add.u32 a, %1, 40;\n\tadd.s64 b, %2, %7;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
+               "}"
+               :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc0),
+                  "n"(1 * OB), "n"(2 * OB), "n"(3 * OB)
+               : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -215,14 +271,14 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const AttnBwdParams p) {
 // dK/dV and dQ kernels
 // ---------------------------------------------------------------------------
 
-template <int D>
+template <int D, int Mode>
 __device__ __forceinline__ void bwd_teardown(uint32_t* tmem_slot, int warp) {
   tc_fence_before();
   asm volatile("bar.sync 1, %0;" ::"n"(kBwdThreads) : "memory");
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(*reinterpret_cast<volatile uint32_t*>(tmem_slot), BwdLayout<D>::kTmemCols);
+    tmem_dealloc(*reinterpret_cast<volatile uint32_t*>(tmem_slot), BwdLayout<D, Mode>::kTmemCols);
   }
 }
 
@@ -255,7 +311,7 @@ template <int D, int Mode, typename IdxT>
 __device__ __forceinline__ void bwd_producer_roles(const AttnBwdParams& p, const CUtensorMap& tr1,
                                                    const CUtensorMap& tr2, const CUtensorMap& tc1,
                                                    const CUtensorMap& tc2) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, Mode>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -264,30 +320,30 @@ __device__ __forceinline__ void bwd_producer_roles(const AttnBwdParams& p, const
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
   BwdMeta* meta = reinterpret_cast<BwdMeta*>(smem + L::kMeta);
   uint8_t* slots = smem + L::kSlots;
+  volatile int* stage_flags = reinterpret_cast<volatile int*>(smem + L::kStageFlags);
+  volatile int* buf_flags = reinterpret_cast<volatile int*>(smem + L::kBufFlags);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int T = static_cast<int>(p.T);
   const Sync sy{bars, abort_flag, p.timeout_ns, &p.ws->error_word, lane};
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::NS; ++i) {
-      mbar_init(&bars[bC1Full + i], 1);
-      mbar_init(&bars[bC1Empty + i], 1);
-      mbar_init(&bars[bC2Full + i], 1);
-      mbar_init(&bars[bC2Empty + i], 1);
+      mbar_init(&bars[bCFull + i], 2);
+      mbar_init(&bars[bCEmpty + i], 1);
     }
     for (int i = 0; i < kBwdMeta; ++i) {
       mbar_init(&bars[bMFull + i], 1);
-      mbar_init(&bars[bMEmpty + i], kBwdMEmptyCount);
     }
     mbar_init(&bars[bRFull], 1);
     mbar_init(&bars[bREmpty], 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kMaxBufs; ++i) {
       mbar_init(&bars[bSFull + i], 1);
-      mbar_init(&bars[bPFull + i], 128);
+      mbar_init(&bars[bPFull + i], kBwdEwWarps);
+      mbar_init(&bars[bTSDone + i], 1);
     }
     mbar_init(&bars[bAccFull], 1);
-    mbar_init(&bars[bAccEmpty], 128);
-    mbar_init(&bars[bDrain], 1);
+    mbar_init(&bars[bAccEmpty], kBwdEwWarps);
+    for (int i = 0; i < 2; ++i) mbar_init(&bars[bDrain + i], 1);
     *abort_flag = 0;
     mbar_fence_init();
     tma_prefetch_desc(&tr1);
@@ -321,7 +377,6 @@ __device__ __forceinline__ void bwd_producer_roles(const AttnBwdParams& p, const
 
     auto push_meta = [&](int flags, int cls, int c0, int r0, int b, int h, int kvh,
                          int mh) -> bool {
-      if (!sy.warp(bMEmpty + mslot, (mround & 1) ^ 1)) return false;
       if (!(flags & kStop)) {
         uint8_t* sd = slots + mslot * kSlotBytes;
         if (Mode == kModeDQ) {
@@ -400,14 +455,15 @@ __device__ __forceinline__ void bwd_producer_roles(const AttnBwdParams& p, const
         r_armed = r_round;
         ++r_round;
       }
-      if (!sy.warp(bC1Empty + cst, (cround & 1) ^ 1)) return false;
+      if (!sy.warp(bCEmpty + cst, (cround & 1) ^ 1)) return false;
       if (lane == 0) {
         const int cx = (Mode == kModeDQ ? kvh : h) * D;
-        mbar_arrive_expect_tx(&bars[bC1Full + cst], L::kCBytes);
+        stage_flags[cst] = flags;
+        mbar_arrive_expect_tx(&bars[bCFull + cst], L::kCBytes);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_2d(smem + L::kC1 + cst * L::kCBytes + c * (kSub * 128), &tc1,
-                      &bars[bC1Full + cst], cx + c * 64, c0);
+                      &bars[bCFull + cst], cx + c * 64, c0);
       }
       c_armed[cst] = cround;
       if (++cst == L::NS) {
@@ -422,7 +478,14 @@ __device__ __forceinline__ void bwd_producer_roles(const AttnBwdParams& p, const
       if (lane == 0) item = static_cast<int64_t>(atomicAdd(counter, 1u));
       item = __shfl_sync(0xffffffffu, item, 0);
       if (item >= n_items) {
-        ok = push_meta(kStop, kClsF, 0, 0, 0, 0, 0, 0);
+        // the stop token: through the metadata ring (C2 producer,
+        // elementwise warps) and through the next stage (issuers)
+        ok = push_meta(kStop, kClsF, 0, 0, 0, 0, 0, 0) &&
+             sy.warp(bCEmpty + cst, (cround & 1) ^ 1);
+        if (ok && lane == 0) {
+          stage_flags[cst] = kStop;
+          mbar_arrive(&bars[bCFull + cst]);
+        }
         break;
       }
       // dQ: slots in reverse order (the later Q tiles of a causal sample
@@ -525,11 +588,11 @@ __device__ __forceinline__ void bwd_producer_roles(const AttnBwdParams& p, const
       // let every TMA load this warp issued land before the CTA exits
       for (int st = 0; st < L::NS; ++st)
         if (c_armed[st] != 0xffffffffu)
-          mbar_wait_bounded(&bars[bC1Full + st], c_armed[st] & 1, 100000000ull, nullptr);
+          mbar_wait_bounded(&bars[bCFull + st], c_armed[st] & 1, 100000000ull, nullptr);
       if (r_armed != 0xffffffffu)
         mbar_wait_bounded(&bars[bRFull], r_armed & 1, 100000000ull, nullptr);
     }
-    bwd_teardown<D>(tmem_slot, warp);
+    bwd_teardown<D, Mode>(tmem_slot, warp);
     return;
   } else if (warp == 2) {
     // ------------------------------------------------------------ C2 producer
@@ -544,19 +607,21 @@ __device__ __forceinline__ void bwd_producer_roles(const AttnBwdParams& p, const
         const int c0 = *reinterpret_cast<volatile int*>(&meta[mslot].c0);
         const int h = *reinterpret_cast<volatile int*>(&meta[mslot].h);
         const int kvh = *reinterpret_cast<volatile int*>(&meta[mslot].kvh);
-        mbar_arrive(&bars[bMEmpty + mslot]);
         if (++mslot == kBwdMeta) {
           mslot = 0;
           ++mround;
         }
-        if (flags & kStop) break;
-        if (!sy.lone(bC2Empty + cst, (cround & 1) ^ 1)) { ok = false; break; }
+        if (!sy.lone(bCEmpty + cst, (cround & 1) ^ 1)) { ok = false; break; }
+        if (flags & kStop) {
+          mbar_arrive(&bars[bCFull + cst]);  // second arrival of the stop stage
+          break;
+        }
         const int cx = (Mode == kModeDQ ? kvh : h) * D;
-        mbar_arrive_expect_tx(&bars[bC2Full + cst], L::kCBytes);
+        mbar_arrive_expect_tx(&bars[bCFull + cst], L::kCBytes);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_2d(smem + L::kC2 + cst * L::kCBytes + c * (kSub * 128), &tc2,
-                      &bars[bC2Full + cst], cx + c * 64, c0);
+                      &bars[bCFull + cst], cx + c * 64, c0);
         c_armed[cst] = cround;
         if (++cst == L::NS) {
           cst = 0;
@@ -566,132 +631,137 @@ __device__ __forceinline__ void bwd_producer_roles(const AttnBwdParams& p, const
       if (!ok) {
         for (int st = 0; st < L::NS; ++st)
           if (c_armed[st] != 0xffffffffu)
-            mbar_wait_bounded(&bars[bC2Full + st], c_armed[st] & 1, 100000000ull, nullptr);
+            mbar_wait_bounded(&bars[bCFull + st], c_armed[st] & 1, 100000000ull, nullptr);
       }
     }
-    bwd_teardown<D>(tmem_slot, warp);
+    bwd_teardown<D, Mode>(tmem_slot, warp);
     return;
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 3) {
+    // ----------------------------------------------------------- MMA issuers
+    // Warp 1 issues X / Y of every step, warp 3 the accumulating MMAs; the
+    // whole warp runs each loop, elect.sync picks the issuing lane.  While one
+    // issuer waits on a barrier or commits, the other's MMAs keep the tensor
+    // pipe busy.  Cross-issuer order: X / Y of step t overwrite the buffer the
+    // accumulating MMAs of step t-NB read, so warp 1 waits for their
+    // completion (TSDone); the accumulating MMAs of step t read P / dS of
+    // step t, whose elementwise pass started after X / Y of step t were
+    // complete.  All accumulation comes from one thread, in step order.
     constexpr uint32_t kIdescXY = idesc_bf16_f32(kRes, kSub, false);
     constexpr uint32_t kIdescAcc = idesc_bf16_f32(kRes, D, true);
     const uint32_t r_addr = smem_u32(smem + L::kR);
     const uint32_t c1_addr = smem_u32(smem + L::kC1);
     const uint32_t c2_addr = smem_u32(smem + L::kC2);
-    // K-major operands of X / Y; MN-major streamed operands of the
-    // accumulating MMAs (N = D across the 64-column chunks, K = rows)
-    const uint64_t r1_desc = sdesc_sw128(r_addr, 16, 1024);
-    const uint64_t r2_desc = sdesc_sw128(r_addr + L::kRBytes, 16, 1024);
-    const uint64_t c1_desc = sdesc_sw128(c1_addr, 16, 1024);
-    const uint64_t c2_desc = sdesc_sw128(c2_addr, 16, 1024);
-    const uint64_t c1_mn = sdesc_sw128(c1_addr, kSub * 128, 1024);
-    const uint64_t c2_mn = sdesc_sw128(c2_addr, kSub * 128, 1024);
-    constexpr int RC = (kRes * 128) >> 4;  // next 64-column chunk of a resident tile
-    constexpr int CC = (kSub * 128) >> 4;  // next 64-column chunk of a streamed tile
-    constexpr int KS = (16 * 128) >> 4;    // 16 streamed rows (one K step)
-    uint32_t mslot = 0, mround = 0;
-    uint32_t ss_st = 0, ss_round = 0, ts_st = 0;
-    uint32_t r_round = 0, acc_round = 0;
-    bool acc_pending = false;
-    uint32_t n_ss = 0, n_ts = 0;
-    uint32_t rec = 0;  // 4-bit flags of the (at most two) steps with X/Y issued, not yet accumulated
-    bool stopped = false, ok = true;
-
-    auto issue_xy = [&](uint32_t xb, uint32_t st) {
-      const uint64_t cd1 = c1_desc + static_cast<uint64_t>(st * (L::kCBytes >> 4));
-      const uint64_t cd2 = c2_desc + static_cast<uint64_t>(st * (L::kCBytes >> 4));
-      if constexpr (D == 128) {
-        umma_ss_group8<2, 2, 4, 4, 6, 6, RC, CC, RC + 2, CC + 2, RC + 4, CC + 4, RC + 6, CC + 6>(
-            tmem_base + L::x_col(xb), r1_desc, cd1, kIdescXY, 0u);
-        umma_ss_group8<2, 2, 4, 4, 6, 6, RC, CC, RC + 2, CC + 2, RC + 4, CC + 4, RC + 6, CC + 6>(
-            tmem_base + L::y_col(xb), r2_desc, cd2, kIdescXY, 0u);
-      } else {
-        umma_ss_group4<2, 2, 4, 4, 6, 6>(tmem_base + L::x_col(xb), r1_desc, cd1, kIdescXY, 0u);
-        umma_ss_group4<2, 2, 4, 4, 6, 6>(tmem_base + L::y_col(xb), r2_desc, cd2, kIdescXY, 0u);
-      }
-    };
-    auto issue_acc = [&](uint32_t xb, uint32_t st, bool first) {
-      const uint64_t m1 = c1_mn + static_cast<uint64_t>(st * (L::kCBytes >> 4));
-      const uint64_t m2 = c2_mn + static_cast<uint64_t>(st * (L::kCBytes >> 4));
-      const uint32_t acc = first ? 0u : 1u;
-      if (Mode == kModeDQ) {
-        // dQ += dS K
-        umma_ts_group4<KS>(tmem_base + L::kAcc0, tmem_base + L::y_col(xb), m1, kIdescAcc, acc);
-      } else {
-        // dV += P^T dO, dK += dS^T Q
-        umma_ts_group4<KS>(tmem_base + L::kAcc0, tmem_base + L::x_col(xb), m2, kIdescAcc, acc);
-        umma_ts_group4<KS>(tmem_base + L::kAcc1, tmem_base + L::y_col(xb), m1, kIdescAcc, acc);
-      }
-    };
-
-    while (ok) {
-      // X / Y of up to two steps ahead of the accumulating MMAs
-      while (!stopped && n_ss < n_ts + 2) {
-        if (!sy.warp(bMFull + mslot, mround & 1)) { ok = false; break; }
-        const int flags = *reinterpret_cast<volatile int*>(&meta[mslot].flags);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[bMEmpty + mslot]);
-        if (++mslot == kBwdMeta) {
-          mslot = 0;
-          ++mround;
-        }
-        if (flags & kStop) {
-          stopped = true;
-          break;
-        }
+    const int me = warp == 1 ? 0 : 1;
+    uint32_t st = 0, round = 0, n = 0;  // stage ring position, steps done
+    bool ok = true;
+    if (me == 0) {
+      // K-major operands of X = R1 C1^T and Y = R2 C2^T
+      const uint64_t r1_desc = sdesc_sw128(r_addr, 16, 1024);
+      const uint64_t r2_desc = sdesc_sw128(r_addr + L::kRBytes, 16, 1024);
+      const uint64_t c1_desc = sdesc_sw128(c1_addr, 16, 1024);
+      const uint64_t c2_desc = sdesc_sw128(c2_addr, 16, 1024);
+      constexpr int RC = (kRes * 128) >> 4;  // next 64-column chunk of a resident tile
+      constexpr int CC = (kSub * 128) >> 4;  // next 64-column chunk of a streamed tile
+      uint32_t r_round = 0;
+      for (;;) {
+        // the stage's full barrier also publishes the step's flags
+        if (!sy.warp(bCFull + st, round & 1)) { ok = false; break; }
+        const int flags = stage_flags[st];
+        if (flags & kStop) break;
         if (flags & kFirst) {
           if (!sy.warp(bRFull, r_round & 1)) { ok = false; break; }
           ++r_round;
         }
-        if (!sy.warp(bC1Full + ss_st, ss_round & 1)) { ok = false; break; }
-        if (!sy.warp(bC2Full + ss_st, ss_round & 1)) { ok = false; break; }
+        const uint32_t xb = n % L::NB;
+        if (!sy.warp(bTSDone + xb, ((n / L::NB) & 1u) ^ 1u)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t xb = n_ss & 1u;
-        issue_xy(xb, ss_st);
+        const uint64_t cd1 = c1_desc + static_cast<uint64_t>(st * (L::kCBytes >> 4));
+        const uint64_t cd2 = c2_desc + static_cast<uint64_t>(st * (L::kCBytes >> 4));
+        if constexpr (D == 128) {
+          umma_ss_group8<2, 2, 4, 4, 6, 6, RC, CC, RC + 2, CC + 2, RC + 4, CC + 4, RC + 6, CC + 6>(
+              tmem_base + L::x_col(xb), r1_desc, cd1, kIdescXY, 0u);
+          umma_ss_group8<2, 2, 4, 4, 6, 6, RC, CC, RC + 2, CC + 2, RC + 4, CC + 4, RC + 6, CC + 6>(
+              tmem_base + L::y_col(xb), r2_desc, cd2, kIdescXY, 0u);
+        } else {
+          umma_ss_group4<2, 2, 4, 4, 6, 6>(tmem_base + L::x_col(xb), r1_desc, cd1, kIdescXY, 0u);
+          umma_ss_group4<2, 2, 4, 4, 6, 6>(tmem_base + L::y_col(xb), r2_desc, cd2, kIdescXY, 0u);
+        }
         umma_commit_elect(&bars[bSFull + xb]);
         if (flags & kLast) umma_commit_elect(&bars[bREmpty]);
-        rec = (rec & ~(0xFu << (xb * 4))) | (static_cast<uint32_t>(flags & 0xF) << (xb * 4));
-        ++n_ss;
-        if (++ss_st == L::NS) {
-          ss_st = 0;
-          ++ss_round;
+        ++n;
+        if (++st == L::NS) {
+          st = 0;
+          ++round;
         }
       }
-      if (!ok || n_ts == n_ss) break;
-      const uint32_t xb = n_ts & 1u;
-      const int flags = static_cast<int>((rec >> (xb * 4)) & 0xFu);
-      const bool first = (flags & kFirst) != 0;
-      if (!sy.warp(bPFull + xb, (n_ts >> 1) & 1u)) { ok = false; break; }
-      if (first && acc_pending) {
-        if (!sy.warp(bAccEmpty, acc_round & 1)) { ok = false; break; }
-        ++acc_round;
-        acc_pending = false;
+    } else {
+      // MN-major streamed operands of the accumulating MMAs (N = D across
+      // the 64-column chunks, K = streamed rows)
+      const uint64_t c1_mn = sdesc_sw128(c1_addr, kSub * 128, 1024);
+      const uint64_t c2_mn = sdesc_sw128(c2_addr, kSub * 128, 1024);
+      constexpr int KS = (16 * 128) >> 4;  // 16 streamed rows (one K step)
+      uint32_t acc_round = 0;
+      bool acc_pending = false;
+      for (;;) {
+        // P-full also publishes the step's flags (and the stop token)
+        const uint32_t xb = n % L::NB;
+        if (!sy.warp(bPFull + xb, (n / L::NB) & 1u)) { ok = false; break; }
+        const int flags = buf_flags[xb];
+        if (flags & kStop) break;
+        const bool first = (flags & kFirst) != 0;
+        if (first && acc_pending) {
+          if (!sy.warp(bAccEmpty, acc_round & 1)) { ok = false; break; }
+          ++acc_round;
+          acc_pending = false;
+        }
+        tc_fence_after();
+        const uint64_t m1 = c1_mn + static_cast<uint64_t>(st * (L::kCBytes >> 4));
+        const uint64_t m2 = c2_mn + static_cast<uint64_t>(st * (L::kCBytes >> 4));
+        const uint32_t acc = first ? 0u : 1u;
+        if (Mode == kModeDQ) {
+          // dQ += dS K
+          umma_ts_group4_split<KS>(tmem_base + L::kAcc0, tmem_base + L::y_col(xb), m1, kIdescAcc,
+                                   acc);
+        } else {
+          // dV += P^T dO, dK += dS^T Q
+          umma_ts_group4_split<KS>(tmem_base + L::kAcc0, tmem_base + L::x_col(xb), m2, kIdescAcc,
+                                   acc);
+          umma_ts_group4_split<KS>(tmem_base + L::kAcc1, tmem_base + L::y_col(xb), m1, kIdescAcc,
+                                   acc);
+        }
+        umma_commit_elect(&bars[bTSDone + xb]);
+        umma_commit_elect(&bars[bCEmpty + st]);
+        if (flags & kLast) {
+          umma_commit_elect(&bars[bAccFull]);
+          acc_pending = true;
+        }
+        ++n;
+        if (++st == L::NS) {
+          st = 0;
+          ++round;
+        }
       }
-      tc_fence_after();
-      issue_acc(xb, ts_st, first);
-      umma_commit_elect(&bars[bC1Empty + ts_st]);
-      umma_commit_elect(&bars[bC2Empty + ts_st]);
-      if (flags & kLast) {
-        umma_commit_elect(&bars[bAccFull]);
-        acc_pending = true;
-      }
-      ++n_ts;
-      if (++ts_st == L::NS) ts_st = 0;
     }
-    // all issued MMAs complete before TMEM is released
-    umma_commit_elect(&bars[bDrain]);
-    mbar_wait_bounded(&bars[bDrain], 0, 100000000ull, nullptr);
-    bwd_teardown<D>(tmem_slot, warp);
+    (void)ok;
+    // all MMAs this issuer issued complete before TMEM is released
+    umma_commit_elect(&bars[bDrain + me]);
+    mbar_wait_bounded(&bars[bDrain + me], 0, 100000000ull, nullptr);
+    bwd_teardown<D, Mode>(tmem_slot, warp);
     return;
   } else {
-    bwd_teardown<D>(tmem_slot, warp);  // idle warp
+    bwd_teardown<D, Mode>(tmem_slot, warp);  // idle warp
   }
 }
 
-// Warps 4..7: P, dS and the epilogue.  Thread = TMEM lane = resident row.
+// Warps 4..11: P, dS and the epilogue, two warpgroups.  Both take every
+// step; warpgroup w handles streamed columns [32 w, 32 w + 32) of it, which
+// halves the time from X / Y ready to P / dS written (the part of a step the
+// tensor cores wait for).  Thread = TMEM lane = resident row.  At the end of
+// an item warpgroup 0 writes dQ columns [0, D/2) or dV, warpgroup 1 dQ
+// columns [D/2, D) or dK.
 template <int D, int Mode, typename IdxT>
 __device__ __forceinline__ void bwd_elementwise_role(const AttnBwdParams& p) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, Mode>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -700,6 +770,7 @@ __device__ __forceinline__ void bwd_elementwise_role(const AttnBwdParams& p) {
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
   const BwdMeta* meta = reinterpret_cast<const BwdMeta*>(smem + L::kMeta);
   const uint8_t* slots = smem + L::kSlots;
+  volatile int* buf_flags = reinterpret_cast<volatile int*>(smem + L::kBufFlags);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int T = static_cast<int>(p.T);
@@ -708,6 +779,7 @@ __device__ __forceinline__ void bwd_elementwise_role(const AttnBwdParams& p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const int wg = (warp - 4) >> 2;  // which 32 streamed columns
   const int row = (warp & 3) * 32 + lane;
   const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const bool causal = p.causal != 0;
@@ -722,7 +794,17 @@ __device__ __forceinline__ void bwd_elementwise_role(const AttnBwdParams& p) {
     const int4 ma = *reinterpret_cast<const int4*>(meta + mslot);      // flags, cls, c0, r0
     const int4 mb = *(reinterpret_cast<const int4*>(meta + mslot) + 1);  // b, h, kvh, mh
     const int flags = ma.x;
-    if (flags & kStop) break;
+    const uint32_t xb = n_steps % L::NB;
+    if (flags & kStop) {
+      // pass the stop token to the accumulating issuer through the next
+      // buffer, once the issuer has taken the flags of that buffer's previous
+      // step (its MMAs for that step are done)
+      if (!sy.warp(bTSDone + xb, ((n_steps / L::NB) & 1u) ^ 1u)) break;
+      if (warp == 4 && lane == 0) buf_flags[xb] = kStop;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[bPFull + xb]);
+      break;
+    }
     const int cls = ma.y, c0 = ma.z, r0 = ma.w;
     const int b = mb.x, h = mb.y, kvh = mb.z, mh = mb.w;
     const int r = r0 + row;  // resident row of this thread
@@ -731,8 +813,9 @@ __device__ __forceinline__ void bwd_elementwise_role(const AttnBwdParams& p) {
       mslot = 0;
       ++mround;
     }
-    // element mask of the 64 streamed columns (bit set = masked)
-    uint32_t mbits[2] = {0u, 0u};
+    // element mask of this warpgroup's 32 streamed columns (bit set = masked)
+    uint32_t mbits = 0u;
+    const int cw = c0 + 32 * wg;  // first column of the warpgroup
     if (Mode == kModeDQ) {
       if (flags & kFirst) {
         nl_row = -CUDART_INF_F;
@@ -743,45 +826,36 @@ __device__ __forceinline__ void bwd_elementwise_role(const AttnBwdParams& p) {
           nd_row = __ldg(p.ndelta + o);
         }
       }
-      // columns = keys c0 + jj; from `valid` on they are outside the sample
-      const int valid = min(kSub, b - c0);
+      // columns = keys cw + j; from `valid` on they are outside the sample
+      const int valid = b - cw;
       if (cls == kClsPC) {
-#pragma unroll
-        for (int w = 0; w < 2; ++w)
-          mbits[w] = range_bits(r - c0 + 1, kSub, w) | range_bits(valid, kSub, w);
+        mbits = range_bits(r - cw + 1, 32, 0) | range_bits(valid, 32, 0);
       } else if (cls == kClsP) {
-        const int* cl = reinterpret_cast<const int*>(slots + cur_slot * kSlotBytes);
+        const int* cl = reinterpret_cast<const int*>(slots + cur_slot * kSlotBytes) + 32 * wg;
 #pragma unroll
-        for (int w = 0; w < 2; ++w) {
-          uint32_t bits = 0;
+        for (int i = 0; i < 32; i += 4) {
+          const int4 a4 = *reinterpret_cast<const int4*>(cl + i);
+          const int4 e4 = *reinterpret_cast<const int4*>(cl + kSub + i);
+          const int4 ua4 = *reinterpret_cast<const int4*>(cl + 2 * kSub + i);
+          const int4 ue4 = *reinterpret_cast<const int4*>(cl + 3 * kSub + i);
+          const int av[4] = {a4.x, a4.y, a4.z, a4.w};
+          const int ev[4] = {e4.x, e4.y, e4.z, e4.w};
+          const int uav[4] = {ua4.x, ua4.y, ua4.z, ua4.w};
+          const int uev[4] = {ue4.x, ue4.y, ue4.z, ue4.w};
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const int jj = w * 32 + i;
-            const int4 a4 = *reinterpret_cast<const int4*>(cl + jj);
-            const int4 e4 = *reinterpret_cast<const int4*>(cl + kSub + jj);
-            const int4 ua4 = *reinterpret_cast<const int4*>(cl + 2 * kSub + jj);
-            const int4 ue4 = *reinterpret_cast<const int4*>(cl + 3 * kSub + jj);
-            const int av[4] = {a4.x, a4.y, a4.z, a4.w};
-            const int ev[4] = {e4.x, e4.y, e4.z, e4.w};
-            const int uav[4] = {ua4.x, ua4.y, ua4.z, ua4.w};
-            const int uev[4] = {ue4.x, ue4.y, ue4.z, ue4.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const bool lower = r >= c0 + jj + q;
-              const bool in_lt = (av[q] <= r) & (r < ev[q]);
-              const bool in_ut = causal | ((uav[q] <= r) & (r < uev[q]));
-              const bool m = (jj + q >= valid) | (lower ? in_lt : in_ut);
-              bits |= static_cast<uint32_t>(m) << (i + q);
-            }
+          for (int q = 0; q < 4; ++q) {
+            const bool lower = r >= cw + i + q;
+            const bool in_lt = (av[q] <= r) & (r < ev[q]);
+            const bool in_ut = causal | ((uav[q] <= r) & (r < uev[q]));
+            const bool m = (i + q >= valid) | (lower ? in_lt : in_ut);
+            mbits |= static_cast<uint32_t>(m) << (i + q);
           }
-          mbits[w] = bits;
         }
       } else {
-#pragma unroll
-        for (int w = 0; w < 2; ++w) mbits[w] = range_bits(valid, kSub, w);
+        mbits = range_bits(valid, 32, 0);
       }
     } else {
-      // columns = queries c0 + jj; rows outside the sample already carry
+      // columns = queries cw + j; rows outside the sample already carry
       // -lse*log2(e) = -inf
       if (flags & kFirst) cur_mh = -1;  // new key rows
       if (cls == kClsP && mh != cur_mh) {
@@ -797,58 +871,61 @@ __device__ __forceinline__ void bwd_elementwise_role(const AttnBwdParams& p) {
       }
       if (cls == kClsPC) {
         // query rows above the key (i < j) are masked
-#pragma unroll
-        for (int w = 0; w < 2; ++w) mbits[w] = range_bits(0, r - c0, w);
+        mbits = range_bits(0, r - cw, 0);
       } else if (cls == kClsP) {
         // i >= j: masked iff LTS <= i < LTE; i < j: iff causal or UTS <= i < UTE
-        const int lo0 = max(lts, r) - c0, lo1 = lte - c0;
-        const int up0 = causal ? 0 : uts - c0;
-        const int up1 = (causal ? r : min(ute, r)) - c0;
-#pragma unroll
-        for (int w = 0; w < 2; ++w) mbits[w] = range_bits(lo0, lo1, w) | range_bits(up0, up1, w);
+        const int lo0 = max(lts, r) - cw, lo1 = lte - cw;
+        const int up0 = causal ? 0 : uts - cw;
+        const int up1 = (causal ? r : min(ute, r)) - cw;
+        mbits = range_bits(lo0, lo1, 0) | range_bits(up0, up1, 0);
       }
     }
 
-    const uint32_t xb = n_steps & 1u;
-    if (!sy.warp(bSFull + xb, (n_steps >> 1) & 1u)) break;
+    if (!sy.warp(bSFull + xb, (n_steps / L::NB) & 1u)) break;
     tc_fence_after();
     const uint32_t x_t = tmem_base + lane_addr + L::x_col(xb);
     const uint32_t y_t = tmem_base + lane_addr + L::y_col(xb);
-    const float* nl_col = reinterpret_cast<const float*>(slots + cur_slot * kSlotBytes);
-    const float* nd_col = nl_col + kSub;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    {
       uint32_t xr[32], yr[32];
-      tmem_ld32(x_t + half * 32, xr);
-      tmem_ld32(y_t + half * 32, yr);
-      const uint32_t mw = mbits[half];
+      tmem_ld32_pair(x_t + 32 * wg, y_t + 32 * wg, xr, yr);
+      if (mbits != 0u) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if ((mw >> j) & 1u) xr[j] = __float_as_uint(-CUDART_INF_F);
+        for (int j = 0; j < 32; ++j)
+          if ((mbits >> j) & 1u) xr[j] = __float_as_uint(-CUDART_INF_F);
+      }
+      const float* nl_col = reinterpret_cast<const float*>(slots + cur_slot * kSlotBytes) + 32 * wg;
+      const float* nd_col = nl_col + kSub;
       uint32_t pk[16], dk[16];
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        uint64_t nl2, nd2;
+      for (int j = 0; j < 32; j += 4) {
+        uint64_t nl2a, nl2b, nd2a, nd2b;
         if (Mode == kModeDQ) {
-          nl2 = pack_f32x2(nl_row, nl_row);
-          nd2 = pack_f32x2(nd_row, nd_row);
+          nl2a = nl2b = pack_f32x2(nl_row, nl_row);
+          nd2a = nd2b = pack_f32x2(nd_row, nd_row);
         } else {
-          const float2 a2 = *reinterpret_cast<const float2*>(nl_col + half * 32 + j);
-          const float2 d2 = *reinterpret_cast<const float2*>(nd_col + half * 32 + j);
-          nl2 = pack_f32x2(a2.x, a2.y);
-          nd2 = pack_f32x2(d2.x, d2.y);
+          const float4 a4 = *reinterpret_cast<const float4*>(nl_col + j);
+          const float4 d4 = *reinterpret_cast<const float4*>(nd_col + j);
+          nl2a = pack_f32x2(a4.x, a4.y);
+          nl2b = pack_f32x2(a4.z, a4.w);
+          nd2a = pack_f32x2(d4.x, d4.y);
+          nd2b = pack_f32x2(d4.z, d4.w);
         }
-        bwd_pair(xr[j], xr[j + 1], yr[j], yr[j + 1], c2, nl2, nd2, pk[j >> 1], dk[j >> 1]);
+        bwd_pair(xr[j], xr[j + 1], yr[j], yr[j + 1], c2, nl2a, nd2a, pk[j >> 1], dk[j >> 1]);
+        bwd_pair(xr[j + 2], xr[j + 3], yr[j + 2], yr[j + 3], c2, nl2b, nd2b, pk[(j >> 1) + 1],
+                 dk[(j >> 1) + 1]);
       }
-      if (Mode == kModeDKV) tmem_st16(x_t + half * 16, pk);
-      tmem_st16(y_t + half * 16, dk);
+      // bf16 pairs of columns [32 w, 32 w + 32) go to packed columns
+      // [32 w, 32 w + 16): each warpgroup overwrites only columns it has
+      // read itself.  The accumulating MMAs read the packed operand at
+      // column offsets 0, 8 (streamed rows 0..31) and 32, 40 (rows 32..63).
+      if (Mode == kModeDKV) tmem_st16(x_t + 32 * wg, pk);
+      tmem_st16(y_t + 32 * wg, dk);
     }
     tmem_st_wait();
     tc_fence_before();
-    mbar_arrive(&bars[bPFull + xb]);
-    // metadata and per-step data of this step are no longer needed
+    if (warp == 4 && lane == 0) buf_flags[xb] = flags;
     __syncwarp();
-    if (lane == 0) mbar_arrive(&bars[bMEmpty + cur_slot]);
+    if (lane == 0) mbar_arrive(&bars[bPFull + xb]);
 
     if (flags & kLast) {
       if (!sy.warp(bAccFull, acc_cnt & 1u)) break;
@@ -858,41 +935,41 @@ __device__ __forceinline__ void bwd_elementwise_role(const AttnBwdParams& p) {
       const int heads = Mode == kModeDQ ? p.hq : p.hkv;
       const int hh = Mode == kModeDQ ? h : kvh;
       const IdxT off = (static_cast<IdxT>(store ? r : 0) * heads + hh) * static_cast<IdxT>(D);
-      const int n_acc = Mode == kModeDQ ? 1 : 2;
+      // dQ columns [wg D/2, wg D/2 + D/2) (scaled); dV (unscaled) or dK (scaled)
+      constexpr int kCols = Mode == kModeDQ ? D / 2 : D;
+      const float f = (Mode == kModeDKV && wg == 0) ? 1.f : p.scale;
+      __nv_bfloat16* dst =
+          static_cast<__nv_bfloat16*>(Mode == kModeDQ ? p.dq : (wg == 0 ? p.dv : p.dk)) + off +
+          (Mode == kModeDQ ? wg * (D / 2) : 0);
+      const uint32_t acc_t = tmem_base + lane_addr +
+                             (Mode == kModeDQ ? L::kAcc0 + wg * (D / 2)
+                                              : (wg == 0 ? L::kAcc0 : L::kAcc1));
 #pragma unroll
-      for (int which = 0; which < n_acc; ++which) {
-        // dQ (scaled) / dV (unscaled) from kAcc0, dK (scaled) from kAcc1
-        const float f = (Mode == kModeDKV && which == 0) ? 1.f : p.scale;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(
-                                 Mode == kModeDQ ? p.dq : (which == 0 ? p.dv : p.dk)) +
-                             off;
-        const uint32_t acc_t = tmem_base + lane_addr + (which == 0 ? L::kAcc0 : L::kAcc1);
+      for (int c = 0; c < kCols / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(acc_t + c * 32, rr);
+        if (store) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(acc_t + c * 32, rr);
-          if (store) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              d4[u] = make_uint4(pack_bf16x2(__uint_as_float(rr[8 * u + 0]) * f,
-                                             __uint_as_float(rr[8 * u + 1]) * f),
-                                 pack_bf16x2(__uint_as_float(rr[8 * u + 2]) * f,
-                                             __uint_as_float(rr[8 * u + 3]) * f),
-                                 pack_bf16x2(__uint_as_float(rr[8 * u + 4]) * f,
-                                             __uint_as_float(rr[8 * u + 5]) * f),
-                                 pack_bf16x2(__uint_as_float(rr[8 * u + 6]) * f,
-                                             __uint_as_float(rr[8 * u + 7]) * f));
-            }
+          for (int u = 0; u < 4; ++u) {
+            d4[u] = make_uint4(pack_bf16x2(__uint_as_float(rr[8 * u + 0]) * f,
+                                           __uint_as_float(rr[8 * u + 1]) * f),
+                               pack_bf16x2(__uint_as_float(rr[8 * u + 2]) * f,
+                                           __uint_as_float(rr[8 * u + 3]) * f),
+                               pack_bf16x2(__uint_as_float(rr[8 * u + 4]) * f,
+                                           __uint_as_float(rr[8 * u + 5]) * f),
+                               pack_bf16x2(__uint_as_float(rr[8 * u + 6]) * f,
+                                           __uint_as_float(rr[8 * u + 7]) * f));
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(&bars[bAccEmpty]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[bAccEmpty]);
     }
     ++n_steps;
   }
-  bwd_teardown<D>(tmem_slot, warp);
+  bwd_teardown<D, Mode>(tmem_slot, warp);
 }
 
 template <int D, int Mode, typename IdxT>
@@ -911,7 +988,7 @@ template <int D, int Mode, typename IdxT>
 cudaError_t launch_mode(const AttnBwdParams& p, const CUtensorMap& tr1, const CUtensorMap& tr2,
                         const CUtensorMap& tc1, const CUtensorMap& tc2, int num_sms,
                         cudaStream_t stream) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, Mode>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

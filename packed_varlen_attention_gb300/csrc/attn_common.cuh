@@ -326,20 +326,33 @@ __device__ __forceinline__ uint32_t exp2_pair_bf16(uint32_t s0, uint32_t s1, uin
   return packed;
 }
 
+// Sets the CTA's stop flag and the error bit.  The first wait in the grid to
+// expire (not one that gave up because another had already failed) also
+// records where it was: barrier index, parity, block and warp.  Kept out of
+// line: it only runs on the failure path.
+__device__ __noinline__ void sync_fail(volatile int* abort, int* err, int bar, uint32_t parity) {
+  if (*abort == 0 && atomicCAS(err + 1, 0, 1) == 0) {
+    err[2] = bar;
+    err[3] = static_cast<int>(parity);
+    err[4] = static_cast<int>((blockIdx.x << 8) | (threadIdx.x >> 5));
+  }
+  *abort = 1;
+  atomicOr(err, static_cast<int>(FM_DEVERR_TIMEOUT));
+}
+
 struct Sync {
   uint64_t* bars;
   volatile int* abort;
   uint64_t tmo;
-  int* err;
+  int* err;  // device error word; the four ints after it record the first expiry
   int lane;
-  __device__ __forceinline__ void fail() const {
-    *abort = 1;
-    atomicOr(err, static_cast<int>(FM_DEVERR_TIMEOUT));
+  __device__ __forceinline__ void fail(int bar, uint32_t parity) const {
+    sync_fail(abort, err, bar, parity);
   }
   // single-thread wait
   __device__ __forceinline__ bool lone(int bar, uint32_t parity) const {
     if (mbar_wait_bounded(&bars[bar], parity, tmo, abort)) return true;
-    fail();
+    fail(bar, parity);
     return false;
   }
   // every lane waits; the warp proceeds only if all lanes saw the phase.
@@ -348,7 +361,7 @@ struct Sync {
     if (__all_sync(0xffffffffu, mbar_test_wait(&bars[bar], parity))) return true;
     const bool ok = mbar_wait_bounded(&bars[bar], parity, tmo, abort);
     const bool all = __all_sync(0xffffffffu, ok);
-    if (!all && lane == 0) fail();
+    if (!all && lane == 0) fail(bar, parity);
     return all;
   }
 };

@@ -376,6 +376,17 @@ fm_status fm_get_device_error(const void* workspace, int32_t* host_err, void* st
   return FM_OK;
 }
 
+fm_status fm_get_device_timeout_info(const void* workspace, int32_t* host_info, void* stream) {
+  if (workspace == nullptr || host_info == nullptr) return FM_ERR_INVALID_ARG;
+  const auto* hdr = static_cast<const fm::AttnWorkspaceHeader*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(host_info, hdr->diag, sizeof(hdr->diag), cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return FM_ERR_CUDA;
+  return FM_OK;
+}
+
 fm_status fm_debug_bounded_wait(int32_t* device_status, uint64_t timeout_ns, void* stream) {
   if (device_status == nullptr || timeout_ns == 0 || timeout_ns > 1000000000ull)
     return FM_ERR_INVALID_ARG;

@@ -33,9 +33,10 @@ struct AttnWorkspaceHeader {
   int32_t n_qtiles;       // real Q tiles found by the planner
   int32_t n_items;        // work items: (pair of Q tiles) x Hq
   int32_t error_word;     // FM_DEVERR_* bits
+  int32_t diag[4];        // first expired wait: set flag, barrier, parity, block << 8 | warp
   int32_t n_tile_items;   // n_qtiles * Hq
   uint32_t work_counter_kv;  // backward: next key/value work item (atomic)
-  int32_t pad[58];
+  int32_t pad[54];
 };
 static_assert(sizeof(AttnWorkspaceHeader) == 256, "header is 256 bytes");
 

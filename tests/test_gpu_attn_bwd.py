@@ -54,7 +54,8 @@ def run_grad(fm, wl, do_bits, causal=None, force_int64=False, sri="default"):
     dq, dk, dv = fm.attn_bwd_varlen(q, k, v, out, do, lse, cu_t, sri_t, mm, causal=c,
                                     workspace=ws, force_int64=force_int64)
     torch.cuda.synchronize()
-    assert fm.get_device_error(ws) == 0
+    err = fm.get_device_error(ws)
+    assert err == 0, f"device error {err}, first expired wait {fm.get_device_timeout_info(ws)}"
     return dq, dk, dv, out, lse
 
 
