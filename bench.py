@@ -245,7 +245,7 @@ class Batch:
         self.mm128 = self.mm if wl.block_n == 128 else torch.empty(
             (self.sri.shape[0], 8, fm.num_kv_tiles_bound(T, n, 128)), dtype=torch.int32,
             device=device)
-        self.bws = torch.empty(fm.attn_bwd_workspace_size(T, wl.n_heads_q), dtype=torch.uint8,
+        self.bws = torch.empty(fm.attn_bwd_workspace_size(T, n, wl.n_heads_q), dtype=torch.uint8,
                                device=device)
 
     def restore(self):

@@ -232,10 +232,11 @@ FM_API fm_status fm_attn_fwd_varlen_noalloc(const void* q, const void* k, const 
 
 /*
  * fm_attn_bwd_workspace_size -- bytes of device workspace that
- * fm_attn_bwd_varlen needs: a 256-byte header (counters, device error word)
- * and two float arrays of Hq * T.  Returns 0 on invalid arguments.
+ * fm_attn_bwd_varlen needs for these sizes: counters and the device error
+ * word, the scheduler's tables (floor(T / 128) + n_seqs tile slots) and two
+ * float arrays of Hq * T.  Returns 0 on invalid arguments.
  */
-FM_API size_t fm_attn_bwd_workspace_size(int64_t total_tokens, int n_heads_q);
+FM_API size_t fm_attn_bwd_workspace_size(int64_t total_tokens, int n_seqs, int n_heads_q);
 
 /*
  * fm_attn_bwd_varlen -- FlashMask attention backward over packed samples.
@@ -266,7 +267,7 @@ FM_API size_t fm_attn_bwd_workspace_size(int64_t total_tokens, int n_heads_q);
  *   dq                device bf16 [T][Hq][D] (written).
  *   dk, dv            device bf16 [T][Hkv][D] (written).
  *   workspace         device buffer of workspace_bytes >=
- *                     fm_attn_bwd_workspace_size(T, Hq), 256-byte aligned; no
+ *                     fm_attn_bwd_workspace_size(T, n_seqs, Hq), 256-byte aligned; no
  *                     initialisation needed.  Calls that share a workspace
  *                     must be ordered on one stream.  fm_get_device_error
  *                     reads its error word.

@@ -71,7 +71,7 @@ _SIGNATURES = {
                                             ctypes.c_float, _c_int, _c_int, _c_vp, _c_vp, _c_vp,
                                             _c_u32, _c_vp]),
     "fm_attn_fwd_num_work_items": (_c_int, [_c_vp, ctypes.POINTER(_c_i64), _c_vp]),
-    "fm_attn_bwd_workspace_size": (ctypes.c_size_t, [_c_i64, _c_int]),
+    "fm_attn_bwd_workspace_size": (ctypes.c_size_t, [_c_i64, _c_int, _c_int]),
     "fm_attn_bwd_varlen": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_int,
                                     _c_int, _c_int, _c_vp, _c_int, _c_vp, _c_int, _c_vp, _c_int,
                                     ctypes.c_float, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t,
@@ -277,8 +277,8 @@ def attn_fwd_varlen_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     return out, lse
 
 
-def attn_bwd_workspace_size(total_tokens: int, n_heads_q: int) -> int:
-    return int(_lib().fm_attn_bwd_workspace_size(total_tokens, n_heads_q))
+def attn_bwd_workspace_size(total_tokens: int, n_seqs: int, n_heads_q: int) -> int:
+    return int(_lib().fm_attn_bwd_workspace_size(total_tokens, n_seqs, n_heads_q))
 
 
 def attn_bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
@@ -316,7 +316,7 @@ def attn_bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torc
     if dv is None:
         dv = torch.empty_like(v)
     if workspace is None:
-        workspace = torch.empty(attn_bwd_workspace_size(T, hq), dtype=torch.uint8,
+        workspace = torch.empty(attn_bwd_workspace_size(T, n_seqs, hq), dtype=torch.uint8,
                                 device=q.device)
     _check("fm_attn_bwd_varlen", _lib().fm_attn_bwd_varlen(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), T, hq, hkv, d,

@@ -167,6 +167,60 @@ __device__ __forceinline__ void load_stats(const AttnBwdParams& p, int mh, int64
     st[v] = __ldg(p.minmax + (static_cast<int64_t>(mh) * 8 + v) * p.n_kv_slots + slot);
 }
 
+// The 128-row tile of packed slot u (slots: floor(cu[s] / 128) + s + t).
+struct ResTile {
+  int s, a, b;  // sample and its token range [a, b)
+  int r0, r1;   // rows of the tile
+  int64_t t;    // tile index in the sample
+  bool real;    // false for slots that hold no tile
+};
+
+__device__ __forceinline__ ResTile res_tile(const AttnBwdParams& p, int64_t u) {
+  const int T = static_cast<int>(p.T);
+  ResTile rt;
+  rt.s = slot_sample(p, u, kRes);
+  rt.a = clamp_tok(__ldg(p.cu + rt.s), T);
+  rt.b = max(rt.a, clamp_tok(__ldg(p.cu + rt.s + 1), T));
+  rt.t = u - (static_cast<int64_t>(rt.a) / kRes + rt.s);
+  rt.real = rt.t >= 0 && rt.a + rt.t * kRes < rt.b;
+  rt.r0 = rt.real ? rt.a + static_cast<int>(rt.t) * kRes : rt.a;
+  rt.r1 = min(rt.r0 + kRes, rt.b);
+  return rt;
+}
+
+// dQ steps of a Q tile: key tiles of 64 columns up to the diagonal (causal)
+// or the sample end; key tile k covers [a + 64k, min(a + 64k + 64, b)) and
+// takes the statistics of the 128-column tile holding it.
+__device__ __forceinline__ int dq_n_steps(const AttnBwdParams& p, const ResTile& rt) {
+  return p.causal ? (rt.r1 - 1 - rt.a) / kSub + 1 : (rt.b - rt.a + kSub - 1) / kSub;
+}
+__device__ __forceinline__ int dq_class(const AttnBwdParams& p, const ResTile& rt, int mh, int k,
+                                        int n_sub) {
+  if (k >= n_sub) return kClsF;
+  const int c0 = rt.a + k * kSub;
+  const int c1 = min(c0 + kSub, rt.b);
+  int st[8];
+  if (p.sri != nullptr)
+    load_stats(p, mh, static_cast<int64_t>(rt.a / kStatTile) + rt.s + k / 2, st);
+  return classify_block(rt.r0, rt.r1, c0, c1, st, p.sri != nullptr, p.causal != 0);
+}
+
+// dK/dV steps of a key tile, per q head: Q tiles of 64 rows from the one
+// holding the diagonal (causal) or the sample start; step k covers rows
+// [a + 64 (q_first + k), ...).
+__device__ __forceinline__ int dkv_q_first(const AttnBwdParams& p, const ResTile& rt) {
+  return p.causal ? (rt.r0 - rt.a) / kSub : 0;
+}
+__device__ __forceinline__ int dkv_class(const AttnBwdParams& p, const ResTile& rt, int mh, int k,
+                                         int q_first, int n_q) {
+  if (k >= n_q) return kClsF;
+  const int q0 = rt.a + (q_first + k) * kSub;
+  const int q1 = min(q0 + kSub, rt.b);
+  int st[8];
+  if (p.sri != nullptr) load_stats(p, mh, static_cast<int64_t>(rt.a / kStatTile) + rt.s + rt.t, st);
+  return classify_block(q0, q1, rt.r0, rt.r1, st, p.sri != nullptr, p.causal != 0);
+}
+
 // P and dS for two elements: p = 2^(x * c + nl), ds = p * (y + nd); returns
 // both as bf16x2 (first element in the low half).
 __device__ __forceinline__ void bwd_pair(uint32_t x0, uint32_t x1, uint32_t y0, uint32_t y1,
@@ -268,6 +322,74 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const AttnBwdParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// planner: the 128-row tiles of every sample, longest samples first
+// ---------------------------------------------------------------------------
+
+// One CTA.  Samples are ordered by their number of 128-row tiles, longest
+// first (counting sort, lengths capped at kCostBins - 1 tiles); the tiles of
+// a sample stay together, dK/dV in tile order and dQ in reverse tile order,
+// so that under a causal mask the tiles with the most steps come first and
+// the concurrently running items of one sample share their streamed tiles in
+// L2.  Only real tiles are listed.
+template <int Mode>
+__global__ void __launch_bounds__(kCostBins) bwd_plan_order_kernel(const AttnBwdParams p) {
+  __shared__ int tiles_in_bin[kCostBins];
+  __shared__ int warp_tot[kCostBins / 32];
+  const int T = static_cast<int>(p.T);
+  int* order = Mode == kModeDQ ? p.order_q : p.order_kv;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, w = tid >> 5;
+  tiles_in_bin[tid] = 0;
+  __syncthreads();
+  auto n_tiles_of = [&](int s) -> int {
+    const int a = clamp_tok(__ldg(p.cu + s), T);
+    const int b = max(a, clamp_tok(__ldg(p.cu + s + 1), T));
+    return (b - a + kRes - 1) / kRes;
+  };
+  for (int s = tid; s < p.n_seqs; s += kCostBins) {
+    const int n = n_tiles_of(s);
+    if (n > 0) atomicAdd(&tiles_in_bin[min(n, kCostBins - 1)], n);
+  }
+  __syncthreads();
+  // exclusive prefix over bins in descending order (position 0: largest bin)
+  const int bin = kCostBins - 1 - tid;
+  const int cnt = tiles_in_bin[bin];
+  int x = cnt;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, d);
+    if (lane >= d) x += y;
+  }
+  if (lane == 31) warp_tot[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int t = warp_tot[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, d);
+      if (lane >= d) t += y;
+    }
+    warp_tot[lane] = t;
+  }
+  __syncthreads();
+  const int incl = x + (w > 0 ? warp_tot[w - 1] : 0);
+  tiles_in_bin[bin] = incl - cnt;  // now the bin's next free position
+  if (tid == kCostBins - 1) {
+    if (Mode == kModeDQ) p.ws->bwd_q_tiles = incl;
+    else p.ws->bwd_kv_tiles = incl;
+  }
+  __syncthreads();
+  for (int s = tid; s < p.n_seqs; s += kCostBins) {
+    const int n = n_tiles_of(s);
+    if (n == 0) continue;
+    const int pos = atomicAdd(&tiles_in_bin[min(n, kCostBins - 1)], n);
+    const int a = clamp_tok(__ldg(p.cu + s), T);
+    const int base = a / kRes + s;  // slot of the sample's first tile
+    for (int t = 0; t < n; ++t) order[pos + t] = base + (Mode == kModeDQ ? n - 1 - t : t);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // dK/dV and dQ kernels
 // ---------------------------------------------------------------------------
 
@@ -299,12 +421,6 @@ __device__ __forceinline__ void zero_rows(const AttnBwdParams& p, int r0, int r1
       for (int u = 0; u < D / 8; ++u) d1[u] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
-}
-
-// Rows [r0, r1) and columns [c0, c1) of a (query rows, key columns) block.
-__device__ __forceinline__ int block_class(const AttnBwdParams& p, const int (&st)[8], int q0,
-                                           int q1, int k0, int k1) {
-  return classify_block(q0, q1, k0, k1, st, p.sri != nullptr, p.causal != 0);
 }
 
 template <int D, int Mode, typename IdxT>
@@ -364,7 +480,9 @@ __device__ __forceinline__ void bwd_producer_roles(const AttnBwdParams& p, const
     // ------------------------------------------------- producer + metadata
     const int group = p.hq / p.hkv;
     const int n_heads_item = Mode == kModeDQ ? p.hq : p.hkv;
-    const int64_t n_items = p.n_res_slots * n_heads_item;
+    const int64_t n_items =
+        static_cast<int64_t>(Mode == kModeDQ ? p.ws->bwd_q_tiles : p.ws->bwd_kv_tiles) *
+        n_heads_item;
     uint32_t* counter = Mode == kModeDQ ? &p.ws->work_counter : &p.ws->work_counter_kv;
     uint32_t mslot = 0, mround = 0;
     uint32_t cst = 0, cround = 0;
@@ -488,35 +606,19 @@ __device__ __forceinline__ void bwd_producer_roles(const AttnBwdParams& p, const
         }
         break;
       }
-      // dQ: slots in reverse order (the later Q tiles of a causal sample
-      // see the most keys); dK/dV: in order (the first key tiles do)
-      const int64_t u = Mode == kModeDQ ? (p.n_res_slots - 1 - item / n_heads_item)
-                                        : item / n_heads_item;
+      // tiles in the planner's order (longest samples first), heads fastest
+      const int64_t u = __ldg((Mode == kModeDQ ? p.order_q : p.order_kv) + item / n_heads_item);
       const int hi = static_cast<int>(item % n_heads_item);
-      const int s = slot_sample(p, u, kRes);
-      const int a = clamp_tok(__ldg(p.cu + s), T);
-      const int b = max(a, clamp_tok(__ldg(p.cu + s + 1), T));
-      const int64_t t = u - (static_cast<int64_t>(a) / kRes + s);
-      if (t < 0 || a + t * kRes >= b) continue;  // slot without a tile
-      const int r0 = a + static_cast<int>(t) * kRes;
-      const int r1 = min(r0 + kRes, b);
-      const bool has_mask = p.sri != nullptr;
+      const ResTile rt = res_tile(p, u);
+      if (!rt.real) continue;  // (the planner lists real tiles only)
+      const int a = rt.a, b = rt.b, r0 = rt.r0, r1 = rt.r1;
 
       if (Mode == kModeDQ) {
         const int h = hi;
         const int kvh = h / group;
         const int mh = p.hm > 1 ? h : 0;
-        const int n_sub = p.causal ? (r1 - 1 - a) / kSub + 1 : (b - a + kSub - 1) / kSub;
-        // key tile k: columns [a + 64k, min(a + 64k + 64, b)), statistics of
-        // the 128-column tile holding it
-        auto cls_of = [&](int k) -> int {
-          if (k >= n_sub) return kClsF;
-          const int c0 = a + k * kSub;
-          const int c1 = min(c0 + kSub, b);
-          int st[8];
-          if (has_mask) load_stats(p, mh, static_cast<int64_t>(a / kStatTile) + s + k / 2, st);
-          return block_class(p, st, r0, r1, c0, c1);
-        };
+        const int n_sub = dq_n_steps(p, rt);
+        auto cls_of = [&](int k) -> int { return dq_class(p, rt, mh, k, n_sub); };
         int n_live = 0;
         for (int base = 0; base < n_sub; base += 32)
           n_live += __popc(__ballot_sync(0xffffffffu, cls_of(base + lane) != kClsF));
@@ -542,18 +644,10 @@ __device__ __forceinline__ void bwd_producer_roles(const AttnBwdParams& p, const
         }
       } else {
         const int kvh = hi;
-        const int n_qsub = (b - a + kSub - 1) / kSub;
-        const int q_first = p.causal ? (r0 - a) / kSub : 0;
-        const int n_q = n_qsub - q_first;
-        const int64_t sslot = static_cast<int64_t>(a / kStatTile) + s + t;
-        // Q tile q_first + k of q head h: rows [a + 64 (q_first + k), ...)
+        const int q_first = dkv_q_first(p, rt);
+        const int n_q = (b - a + kSub - 1) / kSub - q_first;
         auto cls_of = [&](int h, int k) -> int {
-          if (k >= n_q) return kClsF;
-          const int q0 = a + (q_first + k) * kSub;
-          const int q1 = min(q0 + kSub, b);
-          int st[8];
-          if (has_mask) load_stats(p, p.hm > 1 ? h : 0, sslot, st);
-          return block_class(p, st, q0, q1, r0, r1);
+          return dkv_class(p, rt, p.hm > 1 ? h : 0, k, q_first, n_q);
         };
         int n_live = 0;
         for (int h = kvh * group; h < (kvh + 1) * group; ++h)
@@ -999,6 +1093,9 @@ cudaError_t launch_mode(const AttnBwdParams& p, const CUtensorMap& tr1, const CU
     if (e != cudaSuccess) return e;
     if (dev < 64) configured |= 1ull << dev;
   }
+  bwd_plan_order_kernel<Mode><<<1, kCostBins, 0, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   const int64_t items = p.n_res_slots * (Mode == kModeDQ ? p.hq : p.hkv);
   const int grid = static_cast<int>(items < num_sms ? items : num_sms);
   attn_bwd_kernel<D, Mode, IdxT><<<grid, kBwdThreads, L::kBytes, stream>>>(p, tr1, tr2, tc1, tc2);
@@ -1020,9 +1117,30 @@ cudaError_t launch_all(const AttnBwdParams& p, const BwdMaps& m, int num_sms,
 
 }  // namespace
 
-size_t attn_bwd_workspace_bytes(int64_t T, int n_heads_q) {
-  const size_t bytes = sizeof(AttnWorkspaceHeader) + 2 * static_cast<size_t>(T) * n_heads_q * 4;
+// Workspace: header (cleared per call) | order_q | order_kv (n_slots ints
+// each) | -lse*log2(e) | -delta ([Hq][T] floats each).
+size_t attn_bwd_clear_bytes() { return sizeof(AttnWorkspaceHeader); }
+
+size_t attn_bwd_workspace_bytes(int64_t T, int n_seqs, int n_heads_q) {
+  const int64_t n_slots = T / kRes + n_seqs;
+  size_t bytes = attn_bwd_clear_bytes() + 2 * static_cast<size_t>(n_slots) * sizeof(int);
+  bytes = (bytes + 15) & ~static_cast<size_t>(15);
+  bytes += 2 * static_cast<size_t>(T) * n_heads_q * sizeof(float);
   return (bytes + 255) & ~static_cast<size_t>(255);
+}
+
+void attn_bwd_bind_workspace(AttnBwdParams& p, void* workspace, int64_t T, int n_seqs,
+                             int n_heads_q) {
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int64_t n_slots = T / kRes + n_seqs;
+  p.ws = reinterpret_cast<AttnWorkspaceHeader*>(ws);
+  int* ints = reinterpret_cast<int*>(ws + sizeof(AttnWorkspaceHeader));
+  p.order_q = ints;
+  p.order_kv = ints + n_slots;
+  size_t off = attn_bwd_clear_bytes() + 2 * static_cast<size_t>(n_slots) * sizeof(int);
+  off = (off + 15) & ~static_cast<size_t>(15);
+  p.nlse2 = reinterpret_cast<float*>(ws + off);
+  p.ndelta = p.nlse2 + T * n_heads_q;
 }
 
 cudaError_t launch_attn_bwd(const AttnBwdParams& p, const BwdMaps& maps, bool use_int64,

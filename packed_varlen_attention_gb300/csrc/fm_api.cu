@@ -258,9 +258,9 @@ fm_status fm_attn_fwd_varlen(const void* q, const void* k, const void* v, int64_
   return from_cuda(fm::launch_attn_fwd(p, tq, tk, tv, use64, num_sms, s));
 }
 
-size_t fm_attn_bwd_workspace_size(int64_t total_tokens, int n_heads_q) {
-  if (total_tokens < 0 || n_heads_q < 1) return 0;
-  return fm::attn_bwd_workspace_bytes(total_tokens, n_heads_q);
+size_t fm_attn_bwd_workspace_size(int64_t total_tokens, int n_seqs, int n_heads_q) {
+  if (total_tokens < 0 || n_seqs < 0 || n_heads_q < 1) return 0;
+  return fm::attn_bwd_workspace_bytes(total_tokens, n_seqs, n_heads_q);
 }
 
 fm_status fm_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* out,
@@ -291,7 +291,7 @@ fm_status fm_attn_bwd_varlen(const void* q, const void* k, const void* v, const 
       !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
       !aligned(lse, 4) || !aligned(workspace, 256))
     return FM_ERR_ALIGNMENT;
-  if (workspace_bytes < fm::attn_bwd_workspace_bytes(total_tokens, n_heads_q))
+  if (workspace_bytes < fm::attn_bwd_workspace_bytes(total_tokens, n_seqs, n_heads_q))
     return FM_ERR_WORKSPACE;
   const int64_t n_slots = total_tokens / 128 + n_seqs;
   if (n_slots * n_heads_q >= (int64_t(1) << 31)) return FM_ERR_UNSUPPORTED;
@@ -312,7 +312,6 @@ fm_status fm_attn_bwd_varlen(const void* q, const void* k, const void* v, const 
 
   fm::AttnBwdParams p;
   std::memset(&p, 0, sizeof(p));
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.q = q;
   p.k = k;
   p.v = v;
@@ -325,9 +324,7 @@ fm_status fm_attn_bwd_varlen(const void* q, const void* k, const void* v, const 
   p.cu = cu_seqlens;
   p.sri = startend_row_indices;
   p.minmax = block_minmax;
-  p.ws = reinterpret_cast<fm::AttnWorkspaceHeader*>(ws);
-  p.nlse2 = reinterpret_cast<float*>(ws + sizeof(fm::AttnWorkspaceHeader));
-  p.ndelta = p.nlse2 + total_tokens * n_heads_q;
+  fm::attn_bwd_bind_workspace(p, workspace, total_tokens, n_seqs, n_heads_q);
   p.T = total_tokens;
   p.n_res_slots = n_slots;
   p.n_kv_slots = fm_num_kv_tiles_bound(total_tokens, n_seqs, 128);
@@ -348,7 +345,7 @@ fm_status fm_attn_bwd_varlen(const void* q, const void* k, const void* v, const 
                      total_tokens * n_heads_kv * head_dim >= lim;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, sizeof(fm::AttnWorkspaceHeader), s) != cudaSuccess)
+  if (cudaMemsetAsync(workspace, 0, fm::attn_bwd_clear_bytes(), s) != cudaSuccess)
     return FM_ERR_CUDA;
   return from_cuda(fm::launch_attn_bwd(p, m, use64, num_sms, s));
 }

@@ -36,7 +36,9 @@ struct AttnWorkspaceHeader {
   int32_t diag[4];        // first expired wait: set flag, barrier, parity, block << 8 | warp
   int32_t n_tile_items;   // n_qtiles * Hq
   uint32_t work_counter_kv;  // backward: next key/value work item (atomic)
-  int32_t pad[54];
+  int32_t bwd_q_tiles;       // backward: real 128-row tiles (planner)
+  int32_t bwd_kv_tiles;      // backward: the same count for the key/value pass
+  int32_t pad[52];
 };
 static_assert(sizeof(AttnWorkspaceHeader) == 256, "header is 256 bytes");
 
@@ -93,6 +95,8 @@ struct AttnBwdParams {
   const int32_t* sri;
   const int32_t* minmax;
   AttnWorkspaceHeader* ws;
+  int* order_q;   // [n_res_slots] tile slots in processing order (dQ pass)
+  int* order_kv;  // the same for the key/value pass
   float* nlse2;   // [Hq][T]: -lse * log2(e), -inf for rows with no unmasked key
   float* ndelta;  // [Hq][T]: -(dout . out) per row
   int64_t T;
@@ -113,7 +117,10 @@ struct BwdMaps {
   CUtensorMap q64, do64, k64, v64;
 };
 
-size_t attn_bwd_workspace_bytes(int64_t T, int n_heads_q);
+size_t attn_bwd_workspace_bytes(int64_t T, int n_seqs, int n_heads_q);
+size_t attn_bwd_clear_bytes();
+void attn_bwd_bind_workspace(AttnBwdParams& p, void* workspace, int64_t T, int n_seqs,
+                             int n_heads_q);
 
 cudaError_t launch_attn_bwd(const AttnBwdParams& p, const BwdMaps& maps, bool use_int64,
                             int num_sms, cudaStream_t stream);

@@ -49,7 +49,7 @@ def run_grad(fm, wl, do_bits, causal=None, force_int64=False, sri="default"):
         sri_t = torch.from_numpy(np.ascontiguousarray(sri_np)).cuda()
         mm = fm.mask_block_minmax(sri_t, cu_t, 128)
     out, lse = fm.attn_fwd_varlen(q, k, v, cu_t, sri_t, mm, causal=c, force_int64=force_int64)
-    ws = torch.empty(fm.attn_bwd_workspace_size(wl.total_tokens, wl.n_heads_q),
+    ws = torch.empty(fm.attn_bwd_workspace_size(wl.total_tokens, wl.n_seqs, wl.n_heads_q),
                      dtype=torch.uint8, device="cuda")
     dq, dk, dv = fm.attn_bwd_varlen(q, k, v, out, do, lse, cu_t, sri_t, mm, causal=c,
                                     workspace=ws, force_int64=force_int64)
