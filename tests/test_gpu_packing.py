@@ -94,15 +94,16 @@ def test_pack_equals_samples_alone(fm, causal, block_n):
         assert torch.equal(kr[a:a + n].view(torch.int16), k1.view(torch.int16)), f"rope k, sample {s}"
         assert torch.equal(out[a:a + n].view(torch.int16), o1.view(torch.int16)), f"out, sample {s}"
         assert torch.equal(lse[:, a:a + n], l1), f"lse, sample {s}"
-    # and the pack against the float64 oracle: RoPE on the inputs, attention
-    # on the rotated bf16 values the GPU produced
+    # and the pack against the float64 oracle: RoPE on the inputs, then
+    # attention on the oracle's rotated values stored as bf16 (the in-place
+    # rotation keeps q and k in bf16; nothing here comes from the GPU)
     f64 = gen.bf16_bits_to_f64
-    to_bits = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
-    check_close_bf16(bf16_tensor_to_f64(qr), orope.rope_apply(f64(p.tokens), cu, THETA), 8e-3,
-                     what="pack rope q")
-    check_close_bf16(bf16_tensor_to_f64(kr), orope.rope_apply(f64(kp), cu, THETA), 8e-3,
-                     what="pack rope k")
-    ref_o, ref_l = oat.attention_forward(f64(to_bits(qr)), f64(to_bits(kr)), f64(vp), cu,
+    q_rot = orope.rope_apply(f64(p.tokens), cu, THETA)
+    k_rot = orope.rope_apply(f64(kp), cu, THETA)
+    check_close_bf16(bf16_tensor_to_f64(qr), q_rot, 8e-3, what="pack rope q")
+    check_close_bf16(bf16_tensor_to_f64(kr), k_rot, 8e-3, what="pack rope k")
+    as_bf16 = lambda x: f64(gen.f32_to_bf16_bits(x.astype(np.float32)))
+    ref_o, ref_l = oat.attention_forward(as_bf16(q_rot), as_bf16(k_rot), f64(vp), cu,
                                          p.startend_row_indices, causal)
     check_close_bf16(bf16_tensor_to_f64(out), ref_o, ATTN_MAX_ABS, ATTN_MEAN_ABS, what="pack out")
     check_lse(lse.cpu().numpy().astype(np.float64), ref_l, what="pack lse")
