@@ -49,8 +49,30 @@ from workloads import gen  # noqa: E402
 METRIC = "effective attn TFLOP/s (unmasked FLOPs) & % bf16 peak; RoPE GB/s & % HBM"
 HEADLINE_CFG = 2
 L2_FLUSH_BYTES = 256 << 20   # > 129 MB L2
+L2_FLUSH_NOTE = ("flushed before every timed call: 256 MiB write, then a 256 MiB read so that "
+                 "the write-back of the flush's dirty lines is not charged to the timed kernels")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNELS_PER_STEP = 5  # rope, mask statistics, planner cost, planner order, attention
+
+
+class L2Flush:
+    """Empties L2 between timed calls.
+
+    A write of a buffer larger than L2 leaves L2 full of dirty lines whose
+    write-back would then run inside the next timed kernel (for a short
+    memory-bound kernel that is more traffic than its own).  A read of a
+    second buffer larger than L2 evicts them before the timed region, so the
+    timed kernel starts with a cold, clean L2.
+    """
+
+    def __init__(self, torch, device):
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.acc = torch.zeros((), dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.w.zero_()
+        self.acc.copy_(self.r.sum())
 
 
 # ----------------------------------------------------------------------------
@@ -303,7 +325,7 @@ def time_config(fm, torch, batch, steps, warmup, flush, peaks):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
     for i in range(steps):
         batch.restore()
-        flush.zero_()
+        flush()
         batch.step(fm, events=evs[i])
     torch.cuda.synchronize()
     rope = [e[0].elapsed_time(e[1]) for e in evs]
@@ -325,7 +347,7 @@ def time_backward(fm, torch, batch, steps, warmup, flush):
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
     for i in range(steps):
-        flush.zero_()
+        flush()
         evs[i][0].record()
         batch.backward(fm)
         evs[i][1].record()
@@ -353,7 +375,7 @@ def run_ours(args):
     device = torch.device("cuda", local)
     import packed_varlen_attention_gb300 as fm
     peaks, peak_src = load_peaks()
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    flush = L2Flush(torch, device)
 
     cfgs = [HEADLINE_CFG] if args.configs == "headline" else [1, 2, 3, 4, 5]
     per_config = {}
@@ -412,7 +434,7 @@ def run_ours(args):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     for i in range(args.steps):
         b.restore()
-        flush.zero_()
+        flush()
         b.step(fm, events=evs[i])
     torch.cuda.synchronize()
     if world > 1:
@@ -423,7 +445,7 @@ def run_ours(args):
     e2e_stop = torch.cuda.Event(enable_timing=True)
     e2e_ms = []
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         e2e_start.record()
         b.step_e2e(fm)
         e2e_stop.record()
@@ -484,7 +506,7 @@ def run_ours(args):
             "heads_kv": wl.n_heads_kv, "head_dim": wl.head_dim, "mask": "causal_document",
             "block_m": wl.block_m, "block_n": wl.block_n, "seed": 0,
             "step": "rope_qk_varlen + mask_block_minmax + attn_fwd_varlen",
-            "l2": "flushed before every timed step (256 MiB write)",
+            "l2": L2_FLUSH_NOTE,
             "parallelism": f"replicas x{world}",
         },
         "roofline": {
@@ -628,7 +650,7 @@ def run_sweep(args):
     lse = torch.empty((hq, T), dtype=torch.float32, device=dev)
     ws = torch.empty(fm.attn_fwd_workspace_size(T, 1, hq, blk), dtype=torch.uint8, device=dev)
     counts = torch.zeros(3, dtype=torch.int64, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)
     points = []
     for family, param, causal, sri in gen.sparsity_sweep(T):
         sri_t = torch.from_numpy(sri).to(dev)
@@ -645,7 +667,7 @@ def run_sweep(args):
             call()
         ts = []
         for _ in range(args.steps):
-            flush.zero_()
+            flush()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record()
@@ -671,7 +693,7 @@ def run_sweep(args):
                         "r2": r2}
     line = {"sweep": "sparsity", "tokens": T, "heads_q": hq, "heads_kv": hkv, "head_dim": D,
             "block": blk, "steps": args.steps, "warmup": args.warmup,
-            "l2": "flushed before every timed call (256 MiB write)", "data": "synthetic",
+            "l2": L2_FLUSH_NOTE, "data": "synthetic",
             "points": points, "fits": fits}
     print(json.dumps(line), flush=True)
 
