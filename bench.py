@@ -248,6 +248,7 @@ class Batch:
         self.mm = torch.empty((self.sri.shape[0], 8, fm.num_kv_tiles_bound(T, n, wl.block_n)),
                               dtype=torch.int32, device=device)
         self.out = torch.empty_like(self.q)
+        self.q_rot = torch.empty_like(self.q)
         self.lse = torch.empty((wl.n_heads_q, T), dtype=torch.float32, device=device)
         self.ws = torch.empty(fm.attn_fwd_workspace_size(T, n, wl.n_heads_q, wl.block_m),
                               dtype=torch.uint8, device=device)
@@ -289,6 +290,18 @@ class Batch:
                            class_counts=counts, workspace=self.ws, force_int64=wl.force_int64)
         if events:
             events[3].record()
+
+    def step_fused(self, fm):
+        """The step with RoPE fused into the attention prologue: tile
+        statistics, then one call that rotates the keys in place and every Q
+        tile in shared memory (rotated queries written to q_rot for the
+        backward pass); q itself is not rotated in HBM."""
+        wl = self.wl
+        fm.mask_block_minmax(self.sri, self.cu, wl.block_n, out=self.mm)
+        fm.attn_fwd_varlen_rope(self.q, self.k, self.v, self.cu, wl.theta, self.sri, self.mm,
+                                causal=wl.causal, block_m=wl.block_m, block_n=wl.block_n,
+                                out=self.out, lse=self.lse, q_rot=self.q_rot, workspace=self.ws,
+                                force_int64=wl.force_int64)
 
     def backward(self, fm):
         """Gradients of the step's attention (q, k after RoPE; out, lse of the step)."""
@@ -357,6 +370,34 @@ def time_backward(fm, torch, batch, steps, warmup, flush):
     return float(np.mean([a.elapsed_time(b) for a, b in evs]))
 
 
+def time_fused(fm, torch, batch, steps, warmup, flush):
+    """Mean device time (ms) of the fused-RoPE step, L2 flushed before each."""
+    for _ in range(warmup):
+        batch.restore()
+        batch.step_fused(fm)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for i in range(steps):
+        batch.restore()
+        flush()
+        evs[i][0].record()
+        batch.step_fused(fm)
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    if fm.get_device_error(batch.ws) != 0:
+        raise RuntimeError("fused attention reported a device error")
+    return float(np.mean([a.elapsed_time(b) for a, b in evs]))
+
+
+def fused_entry(fl, fused_ms, step_ms):
+    tf = fl / (fused_ms * 1e-3) / 1e12
+    return {"step_ms": fused_ms, "effective_tflops": tf,
+            "speedup_vs_unfused_step": step_ms / fused_ms,
+            "call": "mask_block_minmax + attn_fwd_varlen_rope (keys rotated in place, Q tiles "
+                    "rotated in shared memory, rotated q written to q_rot)"}
+
+
 def backward_entry(fl, ms, peaks):
     """Backward accounting: 10 * head_dim FLOPs per unmasked pair and q head
     (the five products S, dP, dV, dK, dQ), i.e. 2.5 x the forward count."""
@@ -402,6 +443,8 @@ def run_ours(args):
             "block_counts_fpu": counts.cpu().tolist(),
             "tokens": wl.total_tokens,
         }
+        per_config[gen.CONFIG_NAMES[cfg]]["fused_rope"] = fused_entry(
+            fl, time_fused(fm, torch, b, max(5, min(args.steps, 20)), 3, flush), t["step_ms"])
         per_config[gen.CONFIG_NAMES[cfg]]["backward"] = backward_entry(
             fl, time_backward(fm, torch, b, max(5, min(args.steps, 20)), 3, flush), peaks)
         del b
@@ -451,7 +494,8 @@ def run_ours(args):
         e2e_stop.record()
         e2e_stop.synchronize()
         e2e_ms.append(e2e_start.elapsed_time(e2e_stop))
-    # backward of the same batch (outside the step's timed region)
+    # fused-RoPE variant and backward of the same batch (outside the step's timed region)
+    fused_ms = time_fused(fm, torch, b, args.steps, max(3, args.warmup), flush)
     bwd_ms = time_backward(fm, torch, b, args.steps, max(3, args.warmup), flush)
     clocks = sampler.stop()
 
@@ -486,6 +530,7 @@ def run_ours(args):
         "step_ms": float(np.mean(step_ms)), "effective_tflop_per_step": fl / 1e12,
         "block_counts_fpu": counts.cpu().tolist(), "tokens": wl.total_tokens,
         "backward": backward_entry(fl, bwd_ms, peaks),
+        "fused_rope": fused_entry(fl, fused_ms, float(np.mean(step_ms))),
     }
     line = {
         "metric": METRIC,

@@ -231,6 +231,44 @@ FM_API fm_status fm_attn_fwd_varlen_noalloc(const void* q, const void* k, const 
                                             void* stream);
 
 /*
+ * fm_attn_fwd_varlen_rope -- fm_attn_fwd_varlen with the QK RoPE fused into
+ * the attention prologue.
+ *
+ * Unsloth packing blog, section "Fused QK RoPE Triton kernel with packing":
+ * the rotation Y = X*cos + rotate_half(X)*sin with positions restarting at
+ * every sample start (section "Uncontaminated packing"), fused to save
+ * memory traffic.  Here the queries are never rotated in HBM: every Q tile
+ * is rotated in shared memory right after its load, before the QK^T MMAs
+ * read it.  The keys are rotated in place first (one pass over k only),
+ * because every key tile is read by many Q tiles and the backward pass needs
+ * the rotated keys.  The result (out, lse, block counts) is bit-identical to
+ * fm_rope_qk_varlen(q, k, ..., backward = 0) followed by fm_attn_fwd_varlen:
+ * both use the same rotation arithmetic (frequencies theta^(-2i/D),
+ * channel i paired with i + D/2, angle in extended precision).
+ *
+ * Arguments as fm_attn_fwd_varlen, plus:
+ *   k        device bf16 [T][Hkv][D]: rotated IN PLACE (read and written).
+ *   theta    RoPE base, > 0 and finite (e.g. 10000, 500000, 1e6).
+ *   q        device bf16 [T][Hq][D], NOT rotated: left unchanged unless
+ *            q_rot == q.
+ *   q_rot    optional device bf16 [T][Hq][D], 16-byte aligned: when not NULL
+ *            the rotated queries are written there (every token inside a
+ *            sample, every head), as the backward pass needs them.  May be
+ *            q itself (rotation in place).  NULL: nothing is written.
+ * Errors: as fm_attn_fwd_varlen; theta <= 0, non-finite or k == NULL give
+ * FM_ERR_INVALID_ARG, an unaligned q_rot FM_ERR_ALIGNMENT.
+ */
+FM_API fm_status fm_attn_fwd_varlen_rope(const void* q, void* k, const void* v,
+                                         int64_t total_tokens, int n_heads_q, int n_heads_kv,
+                                         int head_dim, const int32_t* cu_seqlens, int n_seqs,
+                                         double theta, const int32_t* startend_row_indices,
+                                         int n_mask_heads, const int32_t* block_minmax,
+                                         int causal, float softmax_scale, int block_m,
+                                         int block_n, void* out, float* lse, void* q_rot,
+                                         int64_t* block_class_counts, void* workspace,
+                                         size_t workspace_bytes, uint32_t flags, void* stream);
+
+/*
  * fm_attn_bwd_workspace_size -- bytes of device workspace that
  * fm_attn_bwd_varlen needs for these sizes: counters and the device error
  * word, the scheduler's tables (floor(T / 128) + n_seqs tile slots) and two

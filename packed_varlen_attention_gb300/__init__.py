@@ -11,6 +11,7 @@ Entry points (same names as the C ABI in ``include/fm.h``):
 * ``rope_qk_varlen``       fused in-place QK RoPE, positions reset per sample
 * ``mask_block_minmax``    FlashMask per-key-tile min/max of LTS/LTE/UTS/UTE
 * ``attn_fwd_varlen``      FlashMask attention forward (out, lse)
+* ``attn_fwd_varlen_rope``  the same with the QK RoPE fused into its prologue
 * ``attn_bwd_varlen``      FlashMask attention backward (dq, dk, dv)
 """
 
@@ -30,6 +31,7 @@ __all__ = [
     "attn_fwd_workspace_size",
     "attn_fwd_varlen",
     "attn_fwd_varlen_noalloc",
+    "attn_fwd_varlen_rope",
     "attn_fwd_num_work_items",
     "attn_bwd_workspace_size",
     "attn_bwd_varlen",
@@ -70,6 +72,10 @@ _SIGNATURES = {
                                             _c_vp, _c_int, _c_vp, _c_int, _c_vp, _c_int,
                                             ctypes.c_float, _c_int, _c_int, _c_vp, _c_vp, _c_vp,
                                             _c_u32, _c_vp]),
+    "fm_attn_fwd_varlen_rope": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_int, _c_int, _c_int,
+                                         _c_vp, _c_int, ctypes.c_double, _c_vp, _c_int, _c_vp,
+                                         _c_int, ctypes.c_float, _c_int, _c_int, _c_vp, _c_vp,
+                                         _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_u32, _c_vp]),
     "fm_attn_fwd_num_work_items": (_c_int, [_c_vp, ctypes.POINTER(_c_i64), _c_vp]),
     "fm_attn_bwd_workspace_size": (ctypes.c_size_t, [_c_i64, _c_int, _c_int]),
     "fm_attn_bwd_varlen": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_int,
@@ -274,6 +280,60 @@ def attn_fwd_varlen_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
         cu_seqlens.numel() - 1, _ptr(startend_row_indices), hm, _ptr(block_minmax),
         int(bool(causal)), float(softmax_scale), block_m, block_n, _ptr(out), _ptr(lse),
         _ptr(class_counts), FM_FLAG_FORCE_INT64 if force_int64 else 0, _stream(stream)))
+    return out, lse
+
+
+def attn_fwd_varlen_rope(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                         cu_seqlens: torch.Tensor, theta: float,
+                         startend_row_indices: Optional[torch.Tensor] = None,
+                         block_minmax: Optional[torch.Tensor] = None, causal: bool = False,
+                         softmax_scale: float = 0.0, block_m: int = 128, block_n: int = 128,
+                         out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                         q_rot: Optional[torch.Tensor] = None,
+                         class_counts: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None, force_int64: bool = False,
+                         stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Attention forward with the QK RoPE fused into its prologue.
+
+    ``q`` and ``k`` are NOT rotated on entry.  ``k`` is rotated in place;
+    ``q`` is rotated tile by tile in shared memory and left unchanged, unless
+    ``q_rot`` (written with the rotated queries) is ``q`` itself.  Returns
+    (out, lse), bit-identical to ``rope_qk_varlen`` followed by
+    ``attn_fwd_varlen``.
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous [T, H, D]")
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    T, hq, d = q.shape
+    n_seqs = cu_seqlens.numel() - 1
+    hm = 0
+    if startend_row_indices is not None:
+        _need(startend_row_indices, "startend_row_indices", torch.int32)
+        hm = startend_row_indices.shape[0]
+        if block_minmax is None:
+            raise ValueError("block_minmax (from mask_block_minmax) is required with a mask")
+        _need(block_minmax, "block_minmax", torch.int32)
+    if q_rot is not None:
+        _need(q_rot, "q_rot", torch.bfloat16)
+        if q_rot.shape != q.shape or not q_rot.is_contiguous():
+            raise ValueError("q_rot must be a contiguous tensor shaped like q")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((hq, T), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        nbytes = attn_fwd_workspace_size(T, n_seqs, hq, block_m)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if class_counts is not None:
+        _need(class_counts, "class_counts", torch.int64)
+    _check("fm_attn_fwd_varlen_rope", _lib().fm_attn_fwd_varlen_rope(
+        _ptr(q), _ptr(k), _ptr(v), T, hq, k.shape[1], d, _ptr(cu_seqlens), n_seqs,
+        float(theta), _ptr(startend_row_indices), hm, _ptr(block_minmax), int(bool(causal)),
+        float(softmax_scale), block_m, block_n, _ptr(out), _ptr(lse), _ptr(q_rot),
+        _ptr(class_counts), _ptr(workspace), workspace.numel(),
+        FM_FLAG_FORCE_INT64 if force_int64 else 0, _stream(stream)))
     return out, lse
 
 

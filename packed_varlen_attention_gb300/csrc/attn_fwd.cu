@@ -49,9 +49,12 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <cstring>
+
 #include "attn_common.cuh"
 #include "fm_device.cuh"
 #include "fm_internal.h"
+#include "rope_device.cuh"
 
 namespace fm {
 namespace {
@@ -109,7 +112,8 @@ struct TileMeta {
   int r0, r_end;   // query rows of the item [r0, r_end); tile 1 starts at r0 + block_m
   int h, kvh;      // q head, key/value head
   int n_runs;      // partial tiles: runs of equal intervals in the run table, 0 = per column
-  int pad[6];
+  int a;           // first row of the sample (RoPE positions count from it)
+  int pad[5];
 };
 static_assert(sizeof(TileMeta) == 64, "TileMeta is 64 bytes");
 
@@ -129,7 +133,8 @@ enum Bar : int {
   kOEmpty = kPVDone + 4,           // [2] O_i read by the epilogue (128 arrivals)
   kDrain = kOEmpty + 2,            // [2] an issuer's MMAs are all done
   kTurn = kDrain + 2,              // [2] issuer i may issue its next block
-  kNumBars = kTurn + 2
+  kQRot = kTurn + 2,               // [2 tiles][2 buffers] Q_i rotated in place (128 arrivals)
+  kNumBars = kQRot + 4
 };
 
 // arrivals on kMEmpty: the V producer lane, the MMA issuers and the softmax
@@ -347,10 +352,10 @@ __device__ __forceinline__ void attn_teardown(uint32_t* tmem_slot, int warp) {
 
 // Warps 0..3 (reduced register budget): K producer, MMA issuer, V producer
 // and one idle warp; warp 0 initialises the barriers, warp 1 owns TMEM.
-template <int D, int BN, int QT, typename IdxT>
+template <int D, int BN, int QT, typename IdxT, bool ROPE>
 __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const CUtensorMap& tq,
                                                     const CUtensorMap& tk,
-                                                    const CUtensorMap& tv) {
+                                                    const CUtensorMap& tv, const RopeArgs& ra) {
   using L = Layout<D, BN, QT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -387,6 +392,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       mbar_init(&bars[kPVDone + i], 1);
       mbar_init(&bars[kSFull + i], 1);
       mbar_init(&bars[kPFull + i], 128);
+      mbar_init(&bars[kQRot + i], 128);
     }
     mbar_init(&bars[kDrain], 1);
     mbar_init(&bars[kDrain + 1], 1);
@@ -420,7 +426,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
     bool ok = true;
 
     auto push_meta = [&](int flags, int cls0, int cls1, int c0, int c1, int r0, int r_end, int h,
-                         int kvh, bool copy_cols, int mh) -> bool {
+                         int kvh, bool copy_cols, int mh, int a) -> bool {
       if (!sy.warp(kMEmpty + mslot, (mround & 1) ^ 1)) return false;
       int n_runs = 0;
       if (copy_cols) {
@@ -481,6 +487,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         m.r_end = r_end;
         m.h = h;
         m.kvh = kvh;
+        m.a = a;
       }
       __threadfence_block();
       __syncwarp();
@@ -497,7 +504,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       if (lane == 0) item = static_cast<int>(atomicAdd(&p.ws->work_counter, 1u));
       item = __shfl_sync(0xffffffffu, item, 0);
       if (item >= n_items) {
-        ok = push_meta(kStop, kClsF, kClsF, 0, 0, 0, 0, 0, 0, false, 0);
+        ok = push_meta(kStop, kClsF, kClsF, 0, 0, 0, 0, 0, 0, false, 0, 0);
         break;
       }
       const int2 pi = p.order[item / p.hq];
@@ -539,6 +546,31 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
 #pragma unroll
           for (int u = 0; u < D / 8; ++u) dst[u] = make_uint4(0u, 0u, 0u, 0u);
           p.lse[static_cast<IdxT>(h) * static_cast<IdxT>(p.T) + r] = -CUDART_INF_F;
+        }
+        if constexpr (ROPE) {
+          // no Q tile of these rows is loaded: rotate them from q directly
+          if (ra.q_rot != nullptr) {
+            constexpr int kG = D / 16;  // chunk pairs per row
+            for (int idx = lane; idx < (r2 - r0) * kG; idx += 32) {
+              const int r = r0 + idx / kG;
+              const int g = idx % kG;
+              const IdxT off = (static_cast<IdxT>(r) * p.hq + h) * static_cast<IdxT>(D) + g * 8;
+              const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(p.q) + off;
+              __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(ra.q_rot) + off;
+              const uint4 x1 = *reinterpret_cast<const uint4*>(src);
+              const uint4 x2 = *reinterpret_cast<const uint4*>(src + D / 2);
+              const float pos = static_cast<float>(r - a);
+              float cs[8], sn[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                rope_cos_sin(pos, ra.freqs.hi[g * 8 + i], ra.freqs.lo[g * 8 + i], 1.0f, cs[i],
+                             sn[i]);
+              uint4 y1, y2;
+              rope_rotate8(x1, x2, cs, sn, y1, y2);
+              *reinterpret_cast<uint4*>(dst) = y1;
+              *reinterpret_cast<uint4*>(dst + D / 2) = y2;
+            }
+          }
         }
         continue;
       }
@@ -585,7 +617,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
           const int flags = (pushed == 0 ? kFirst : 0) | (pushed == n_live - 1 ? kLast : 0) |
                             (has_q1 ? kHasQ1 : 0);
           const bool copy = (cls0 == kClsP || cls1 == kClsP) && p.sri != nullptr;
-          if (!push_meta(flags, cls0, cls1, c0, c1, r0, r2, h, kvh, copy, mh)) {
+          if (!push_meta(flags, cls0, cls1, c0, c1, r0, r2, h, kvh, copy, mh, a)) {
             ok = false;
             break;
           }
@@ -707,6 +739,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       uint32_t mslot = 0, mround = 0;  // metadata ring (released by the other readers)
       uint32_t kst = 0, kround = 0, vst = 0, vround = 0;
       uint32_t q_round = 0;
+      uint32_t rot_round[2] = {0u, 0u};  // fused RoPE: rotated Q phases awaited per Q buffer
       uint32_t p_round[2] = {0u, 0u}, o_round[2] = {0u, 0u};
       bool o_pending[2] = {false, false};  // an epilogue of tile i has not been waited for
       bool ok = true;
@@ -789,6 +822,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         uint32_t fq = 0u;  // 4-bit flags of the (at most four) tiles with S issued, PV not yet
         uint32_t n_s = 0, n_pv = 0;
         bool s_end = false;
+        bool rot_wait = false;  // fused RoPE: the fetched tile starts an item, Q not yet awaited
         // next tile of the S stream: its metadata, its item's Q buffer (first
         // tile of an item) and its K tile
         auto s_fetch = [&](int& flags) -> bool {
@@ -799,20 +833,36 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
           }
           if (flags & kFirst) {
             qb = q_seq & 1u;
-            if (!sy.warp(kQFull + qb, (q_seq >> 1) & 1u)) return false;
+            if constexpr (ROPE) {
+              // the rotated Q is awaited right before the first S MMA: the
+              // softmax rotates it only after its last P of the previous item
+              rot_wait = true;
+            } else {
+              if (!sy.warp(kQFull + qb, (q_seq >> 1) & 1u)) return false;
+            }
             ++q_seq;
           }
           if (!sy.warp(kKFull + kst, kround & 1)) return false;
           tc_fence_after();
           return true;
         };
-        auto s_one = [&](int i) {
+        auto s_one = [&](int i) -> bool {
+          if constexpr (ROPE) {
+            if (rot_wait) {
+              if (!sy.warp(kQRot + 2 * i + qb, rot_round[qb] & 1u)) return false;
+              ++rot_round[qb];
+              rot_wait = false;
+              tc_fence_after();
+            }
+          }
           const uint32_t sb = s_cnt[i] & 1u;
           issue_s(i, sb, qb);
           umma_commit_elect(&bars[kSFull + 2 * i + sb]);
           ++s_cnt[i];
+          return true;
         };
         auto s_done = [&](int flags) {
+          rot_wait = false;
           umma_commit_elect(&bars[kKEmpty + kst]);
           if (flags & kLast) umma_commit_elect(&bars[kQEmpty + qb]);
           advance_k();
@@ -827,7 +877,10 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
             break;
           }
           if (s_end) break;
-          if (me == 0 || (f & kHasQ1)) s_one(me);
+          if ((me == 0 || (f & kHasQ1)) && !s_one(me)) {
+            ok = false;
+            break;
+          }
           s_done(f);
         }
         while (ok && n_pv < n_s) {
@@ -853,7 +906,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
               ++pv_cnt[i];
               if (last) o_pending[i] = true;
             }
-            if (ahead && (i == 0 || (nxt & kHasQ1))) s_one(i);
+            if (ahead && (i == 0 || (nxt & kHasQ1)) && !s_one(i)) { ok = false; break; }
           }
           umma_commit_elect(&bars[kVEmpty + vst]);
           advance_v();
@@ -885,8 +938,15 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         };
         // S MMAs (all BN key columns) of the first tile of an item
         auto start_item = [&](int flags) -> bool {
-          if (!sy.warp(kQFull, q_round & 1)) return false;
-          ++q_round;
+          if constexpr (ROPE) {
+            if (me == 0 || (flags & kHasQ1)) {
+              if (!sy.warp(kQRot + 2 * me, rot_round[0] & 1)) return false;
+              ++rot_round[0];
+            }
+          } else {
+            if (!sy.warp(kQFull, q_round & 1)) return false;
+            ++q_round;
+          }
           if (!sy.warp(kKFull + kst, kround & 1)) return false;
           tc_fence_after();
           if (!take_turn()) return false;
@@ -970,8 +1030,56 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
 
 // Warps 4..11 (raised register budget): softmax of Q tile 0 (warps 4..7) and
 // of Q tile 1 (warps 8..11).
-template <int D, int BN, int QT, typename IdxT>
-__device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
+// Fused RoPE: rotates row `row` of a Q tile in shared memory (128-byte
+// swizzle: 16-byte chunk j of row r sits at chunk j ^ (r & 7) of the row's
+// 128 bytes; channels [0, 64) in the first 64-column box, [64, 128) in the
+// second).  The row holds a token at position `pos` of its sample.
+template <int D>
+__device__ __forceinline__ void rope_q_tile_row(const RopeArgs& ra, uint32_t tile, int row,
+                                                float pos) {
+  constexpr int kG = D / 16;  // chunk pairs per row
+  const uint32_t row_addr = tile + static_cast<uint32_t>(row) * 128u;
+  const uint32_t sw = static_cast<uint32_t>(row & 7);
+#pragma unroll 2
+  for (int g = 0; g < kG; ++g) {
+    const int g2 = g + kG;
+    const uint32_t a1 = row_addr + (g >> 3) * (kTileM * 128) + (((g & 7) ^ sw) << 4);
+    const uint32_t a2 = row_addr + (g2 >> 3) * (kTileM * 128) + (((g2 & 7) ^ sw) << 4);
+    const uint4 x1 = ld_shared_v4(a1);
+    const uint4 x2 = ld_shared_v4(a2);
+    float cs[8], sn[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      rope_cos_sin(pos, ra.freqs.hi[g * 8 + i], ra.freqs.lo[g * 8 + i], 1.0f, cs[i], sn[i]);
+    uint4 y1, y2;
+    rope_rotate8(x1, x2, cs, sn, y1, y2);
+    st_shared_v4(a1, y1.x, y1.y, y1.z, y1.w);
+    st_shared_v4(a2, y2.x, y2.y, y2.z, y2.w);
+  }
+}
+
+// Copies rows [0, n_rows) of a rotated Q tile from shared memory to
+// q_rot[t0 + row][h] with the 128 threads of a warpgroup (thread `tid`):
+// consecutive threads take consecutive 16-byte chunks of a row, so every
+// warp store covers whole rows.
+template <int D, typename IdxT>
+__device__ __forceinline__ void store_q_tile(const AttnParams& p, const RopeArgs& ra,
+                                             uint32_t tile, int tid, int n_rows, int t0, int h) {
+  constexpr int kC = D / 8;  // 16-byte chunks per row
+  __nv_bfloat16* base = static_cast<__nv_bfloat16*>(ra.q_rot);
+  for (int e = tid; e < n_rows * kC; e += 128) {
+    const int row = e / kC;
+    const int c = e % kC;
+    const uint32_t src =
+        tile + (c >> 3) * (kTileM * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+    const uint4 x = ld_shared_v4(src);
+    *reinterpret_cast<uint4*>(base + (static_cast<IdxT>(t0 + row) * p.hq + h) *
+                                         static_cast<IdxT>(D) + c * 8) = x;
+  }
+}
+
+template <int D, int BN, int QT, typename IdxT, bool ROPE>
+__device__ __forceinline__ void attn_softmax_role(const AttnParams& p, const RopeArgs& ra) {
   using L = Layout<D, BN, QT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -1002,6 +1110,66 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
     uint32_t n_tiles = 0, o_round = 0;  // KV tiles of this warpgroup so far; epilogues
     float m_run = -CUDART_INF_F, l_run = 0.f;
     int rt0 = 0, rt1 = 0, h = 0;
+    uint32_t q_items = 0, item_qb = 0, item_qpar = 0;  // items seen; Q buffer and parity of this one
+    uint32_t rot_cnt[2] = {0u, 0u};  // fused RoPE: Q tiles this warpgroup rotated, per Q buffer
+
+    // Epilogue of an item: once its last PV is done, O / l -> bf16 out rows
+    // (guarded: rows from e_rt1 on belong to the next sample) and lse.
+    // `wait_bar` / `wait_par`: the barrier phase of that last PV.
+    auto epilogue = [&](int e_r, int e_rt1, int e_h, float e_m, float e_l, int wait_bar,
+                        uint32_t wait_par) -> bool {
+      if (!sy.warp(wait_bar, wait_par)) return false;
+      tc_fence_after();
+      const float inv_l = (e_l > 0.f) ? 1.f / e_l : 0.f;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
+                           (static_cast<IdxT>(e_r) * p.hq + e_h) * static_cast<IdxT>(D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(o_tmem + c * 32, rr);
+        if (e_r < e_rt1) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            d4[u] = make_uint4(
+                pack_bf16x2(__uint_as_float(rr[8 * u + 0]) * inv_l,
+                            __uint_as_float(rr[8 * u + 1]) * inv_l),
+                pack_bf16x2(__uint_as_float(rr[8 * u + 2]) * inv_l,
+                            __uint_as_float(rr[8 * u + 3]) * inv_l),
+                pack_bf16x2(__uint_as_float(rr[8 * u + 4]) * inv_l,
+                            __uint_as_float(rr[8 * u + 5]) * inv_l),
+                pack_bf16x2(__uint_as_float(rr[8 * u + 6]) * inv_l,
+                            __uint_as_float(rr[8 * u + 7]) * inv_l));
+          }
+        }
+      }
+      if (e_r < e_rt1) {
+        p.lse[static_cast<IdxT>(e_h) * static_cast<IdxT>(p.T) + e_r] =
+            (e_l > 0.f) ? (e_m + __log2f(e_l)) * 0.69314718055994531f : -CUDART_INF_F;
+      }
+      tc_fence_before();
+      mbar_arrive(&bars[kOEmpty + wg]);
+      return true;
+    };
+    // Fused RoPE defers an item's epilogue until the next item's Q tile is
+    // rotated.  With two S buffers this is required: the MMA issuer waits for
+    // that Q before it issues the item's last PV, which the epilogue waits
+    // for.  With one it lets the rotation overlap the last PV and the next
+    // S MMAs overlap the epilogue.  Until then h, rt0, rt1, m_run and l_run
+    // still hold the item's values; its last tile is tile n_tiles - 1 of this
+    // warpgroup.
+    constexpr bool kDefer = ROPE;
+    bool epi_pending = false;
+    auto flush_epilogue = [&]() -> bool {
+      if (!epi_pending) return true;
+      epi_pending = false;
+      const uint32_t lt = n_tiles - 1u;
+      if constexpr (kBufs<BN, QT> == 2)
+        return epilogue(rt0 + row, rt1, h, m_run, l_run, kPVDone + 2 * wg + (lt & 1u),
+                        (lt >> 1) & 1u);
+      else
+        return epilogue(rt0 + row, rt1, h, m_run, l_run, kOFull + wg, (o_round - 1u) & 1u);
+    };
 
     for (;;) {
       if (!sy.warp(kMFull + mslot, mround & 1)) break;
@@ -1010,15 +1178,29 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
       const int4 ma = *reinterpret_cast<const int4*>(meta + mslot);
       const int4 mb = *(reinterpret_cast<const int4*>(meta + mslot) + 1);
       const int flags = ma.x;
-      if (flags & kStop) break;
+      if (flags & kStop) {
+        if constexpr (kDefer) flush_epilogue();
+        break;
+      }
       const int cls = wg == 0 ? ma.y : ma.z;
       const int c0 = ma.w;
       const int c1 = mb.x;
       const bool first = (flags & kFirst) != 0;
+      // the item's q head and rows (taken over once a deferred epilogue of
+      // the previous item is done)
+      int n_h = h, n_rt0 = rt0, n_rt1 = rt1;
       if (first) {
-        h = mb.w;
-        rt0 = mb.y + wg * BM;
-        rt1 = min(rt0 + BM, mb.z);
+        n_h = mb.w;
+        n_rt0 = mb.y + wg * BM;
+        n_rt1 = min(n_rt0 + BM, mb.z);
+        item_qb = q_items % kBufs<BN, QT>;
+        item_qpar = (q_items / kBufs<BN, QT>) & 1u;
+        ++q_items;
+        if constexpr (!ROPE) {
+          h = n_h;
+          rt0 = n_rt0;
+          rt1 = n_rt1;
+        }
       }
       const uint32_t cur_slot = mslot;
       if (++mslot == kMetaSlots) {
@@ -1028,7 +1210,36 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
       if (wg == 1 && !(flags & kHasQ1)) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kMEmpty + cur_slot]);
+        if constexpr (kDefer) {
+          if (!flush_epilogue()) break;
+        }
         continue;
+      }
+      if constexpr (ROPE) {
+        if (first) {
+          // this warpgroup's Q tile of the item: rotate it in place once it
+          // has landed, then hand it to the tensor cores
+          const int a_start = meta[cur_slot].a;
+          const uint32_t qtile = smem_u32(smem + L::kQ + (item_qb * QT + wg) * L::kQBytes);
+          if (!sy.warp(kQFull + item_qb, item_qpar)) break;
+          rope_q_tile_row<D>(ra, qtile, row, static_cast<float>(max(n_rt0 + row - a_start, 0)));
+          fence_proxy_async_smem();
+          const int rb = kQRot + 2 * wg + static_cast<int>(item_qb);
+          mbar_arrive(&bars[rb]);
+          if (ra.q_rot != nullptr) {
+            // every row of the tile is rotated once the phase completes; the
+            // tile stays in place until this item's last S MMA is done
+            if (!sy.warp(rb, rot_cnt[item_qb] & 1u)) break;
+            store_q_tile<D, IdxT>(p, ra, qtile, row, n_rt1 - n_rt0, n_rt0, n_h);
+          }
+          ++rot_cnt[item_qb];
+          if constexpr (kDefer) {
+            if (!flush_epilogue()) break;
+          }
+          h = n_h;
+          rt0 = n_rt0;
+          rt1 = n_rt1;
+        }
       }
       if (first) {
         m_run = -CUDART_INF_F;
@@ -1199,42 +1410,21 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
       if (flags & kLast) {
         // O_i is final once the PV of this tile is done (MMAs complete in
         // issue order, so every earlier PV is done too)
+        int wbar;
+        uint32_t wpar;
         if constexpr (kBufs<BN, QT> == 2) {
-          if (!sy.warp(kPVDone + 2 * wg + sb, spar)) break;
+          wbar = kPVDone + 2 * wg + sb;
+          wpar = spar;
         } else {
-          if (!sy.warp(kOFull + wg, o_round & 1)) break;
+          wbar = kOFull + wg;
+          wpar = o_round & 1;
         }
         ++o_round;
-        tc_fence_after();
-        const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
-                             (static_cast<IdxT>(r) * p.hq + h) * static_cast<IdxT>(D);
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(o_tmem + c * 32, rr);
-          if (r < rt1) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              d4[u] = make_uint4(
-                  pack_bf16x2(__uint_as_float(rr[8 * u + 0]) * inv_l,
-                              __uint_as_float(rr[8 * u + 1]) * inv_l),
-                  pack_bf16x2(__uint_as_float(rr[8 * u + 2]) * inv_l,
-                              __uint_as_float(rr[8 * u + 3]) * inv_l),
-                  pack_bf16x2(__uint_as_float(rr[8 * u + 4]) * inv_l,
-                              __uint_as_float(rr[8 * u + 5]) * inv_l),
-                  pack_bf16x2(__uint_as_float(rr[8 * u + 6]) * inv_l,
-                              __uint_as_float(rr[8 * u + 7]) * inv_l));
-            }
-          }
+        if constexpr (kDefer) {
+          epi_pending = true;
+        } else {
+          if (!epilogue(r, rt1, h, m_run, l_run, wbar, wpar)) break;
         }
-        if (r < rt1) {
-          p.lse[static_cast<IdxT>(h) * static_cast<IdxT>(p.T) + r] =
-              (l_run > 0.f) ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -CUDART_INF_F;
-        }
-        tc_fence_before();
-        mbar_arrive(&bars[kOEmpty + wg]);
       }
       ++n_tiles;
     }
@@ -1242,19 +1432,20 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p) {
   }
 }
 
-template <int D, int BN, int QT, typename IdxT>
+template <int D, int BN, int QT, typename IdxT, bool ROPE>
 __global__ void __launch_bounds__(kThreads<QT>, 1)
     attn_fwd_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tq,
                     const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv) {
+                    const __grid_constant__ CUtensorMap tv,
+                    const __grid_constant__ RopeArgs ra) {
   // The register split comes first so that no value crosses from one budget
   // into the other.
   if ((threadIdx.x >> 5) < 4) {
     if constexpr (QT == 2) regs_release();
-    attn_producer_roles<D, BN, QT, IdxT>(p, tq, tk, tv);
+    attn_producer_roles<D, BN, QT, IdxT, ROPE>(p, tq, tk, tv, ra);
   } else {
     if constexpr (QT == 2) regs_acquire();
-    attn_softmax_role<D, BN, QT, IdxT>(p);
+    attn_softmax_role<D, BN, QT, IdxT, ROPE>(p, ra);
   }
 }
 
@@ -1271,9 +1462,10 @@ __global__ void bounded_wait_probe_kernel(int32_t* status, uint64_t timeout_ns) 
   if (threadIdx.x == 0) *status = ok ? FM_OK : FM_ERR_TIMEOUT;
 }
 
-template <int D, int BN, int QT, typename IdxT>
+template <int D, int BN, int QT, typename IdxT, bool ROPE>
 cudaError_t launch_typed(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, int num_sms, cudaStream_t stream) {
+                         const CUtensorMap& tv, const RopeArgs& ra, int num_sms,
+                         cudaStream_t stream) {
   using L = Layout<D, BN, QT>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1283,11 +1475,11 @@ cudaError_t launch_typed(const AttnParams& p, const CUtensorMap& tq, const CUten
     // The warpgroups' register split must fit in what the launch allocates,
     // or setmaxnreg.inc would wait forever: refuse to launch otherwise.
     cudaFuncAttributes attr;
-    e = cudaFuncGetAttributes(&attr, attn_fwd_kernel<D, BN, QT, IdxT>);
+    e = cudaFuncGetAttributes(&attr, attn_fwd_kernel<D, BN, QT, IdxT, ROPE>);
     if (e != cudaSuccess) return e;
     if (QT == 2 && attr.numRegs * kThreads<QT> < kProducerRegs * 128 + kSoftmaxRegs * 256)
       return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(attn_fwd_kernel<D, BN, QT, IdxT>,
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D, BN, QT, IdxT, ROPE>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
     if (dev < 64) configured |= 1ull << dev;
@@ -1301,7 +1493,7 @@ cudaError_t launch_typed(const AttnParams& p, const CUtensorMap& tq, const CUten
   if (e != cudaSuccess) return e;
   const int64_t max_items = n_slots * p.hq;
   const int grid = static_cast<int>(max_items < num_sms ? max_items : num_sms);
-  attn_fwd_kernel<D, BN, QT, IdxT><<<grid, kThreads<QT>, L::kBytes, stream>>>(p, tq, tk, tv);
+  attn_fwd_kernel<D, BN, QT, IdxT, ROPE><<<grid, kThreads<QT>, L::kBytes, stream>>>(p, tq, tk, tv, ra);
   return cudaGetLastError();
 }
 
@@ -1314,21 +1506,38 @@ size_t attn_workspace_bytes(int64_t T, int n_seqs, int block_m) {
   return (bytes + 255) & ~static_cast<size_t>(255);
 }
 
-cudaError_t launch_attn_fwd(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, bool use_int64, int num_sms,
-                            cudaStream_t stream) {
+namespace {
+
+template <bool ROPE>
+cudaError_t launch_attn_dispatch(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, const RopeArgs& ra, bool use_int64,
+                                 int num_sms, cudaStream_t stream) {
   if (p.head_dim == 128) {
     if (p.block_n == 128)
-      return use_int64 ? launch_typed<128, 128, kQTilesBN128, int64_t>(p, tq, tk, tv, num_sms, stream)
-                       : launch_typed<128, 128, kQTilesBN128, int32_t>(p, tq, tk, tv, num_sms, stream);
-    return use_int64 ? launch_typed<128, 64, 2, int64_t>(p, tq, tk, tv, num_sms, stream)
-                     : launch_typed<128, 64, 2, int32_t>(p, tq, tk, tv, num_sms, stream);
+      return use_int64
+                 ? launch_typed<128, 128, kQTilesBN128, int64_t, ROPE>(p, tq, tk, tv, ra, num_sms, stream)
+                 : launch_typed<128, 128, kQTilesBN128, int32_t, ROPE>(p, tq, tk, tv, ra, num_sms, stream);
+    return use_int64 ? launch_typed<128, 64, 2, int64_t, ROPE>(p, tq, tk, tv, ra, num_sms, stream)
+                     : launch_typed<128, 64, 2, int32_t, ROPE>(p, tq, tk, tv, ra, num_sms, stream);
   }
   if (p.block_n == 128)
-    return use_int64 ? launch_typed<64, 128, kQTilesBN128, int64_t>(p, tq, tk, tv, num_sms, stream)
-                     : launch_typed<64, 128, kQTilesBN128, int32_t>(p, tq, tk, tv, num_sms, stream);
-  return use_int64 ? launch_typed<64, 64, 2, int64_t>(p, tq, tk, tv, num_sms, stream)
-                   : launch_typed<64, 64, 2, int32_t>(p, tq, tk, tv, num_sms, stream);
+    return use_int64
+               ? launch_typed<64, 128, kQTilesBN128, int64_t, ROPE>(p, tq, tk, tv, ra, num_sms, stream)
+               : launch_typed<64, 128, kQTilesBN128, int32_t, ROPE>(p, tq, tk, tv, ra, num_sms, stream);
+  return use_int64 ? launch_typed<64, 64, 2, int64_t, ROPE>(p, tq, tk, tv, ra, num_sms, stream)
+                   : launch_typed<64, 64, 2, int32_t, ROPE>(p, tq, tk, tv, ra, num_sms, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, bool use_int64, int num_sms,
+                            cudaStream_t stream, const RopeArgs* rope) {
+  if (rope != nullptr)
+    return launch_attn_dispatch<true>(p, tq, tk, tv, *rope, use_int64, num_sms, stream);
+  RopeArgs none;
+  memset(&none, 0, sizeof(none));
+  return launch_attn_dispatch<false>(p, tq, tk, tv, none, use_int64, num_sms, stream);
 }
 
 cudaError_t launch_bounded_wait_probe(int32_t* status, uint64_t timeout_ns, cudaStream_t stream) {

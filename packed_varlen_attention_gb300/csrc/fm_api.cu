@@ -119,7 +119,8 @@ fm_status fm_rope_qk_varlen(void* q, void* k, int64_t total_tokens, int n_heads_
   if (n_heads_kv > 0 && (!aligned(k, 16) || k_token_stride % 8 != 0)) return FM_ERR_ALIGNMENT;
   if (n_heads_q + n_heads_kv > 8 * 65535) return FM_ERR_UNSUPPORTED;
   if (total_tokens == 0) return FM_OK;
-  fm_status st = device_info(nullptr);
+  int num_sms = 0;
+  fm_status st = device_info(&num_sms);
   if (st != FM_OK) return st;
 
   fm::RopeFreqs fr;
@@ -136,7 +137,8 @@ fm_status fm_rope_qk_varlen(void* q, void* k, int64_t total_tokens, int n_heads_
   use64 = use64 || total_tokens * (head_dim / 16) >= lim;
   return from_cuda(fm::launch_rope(q, k, total_tokens, n_heads_q, n_heads_kv, head_dim,
                                    q_token_stride, k_token_stride, cu_seqlens, n_seqs, fr,
-                                   backward != 0, use64, static_cast<cudaStream_t>(stream)));
+                                   backward != 0, use64, num_sms,
+                                   static_cast<cudaStream_t>(stream)));
 }
 
 int64_t fm_num_kv_tiles_bound(int64_t total_tokens, int n_seqs, int block_n) {
@@ -169,14 +171,36 @@ size_t fm_attn_fwd_workspace_size(int64_t total_tokens, int n_seqs, int n_heads_
   return fm::attn_workspace_bytes(total_tokens, n_seqs, block_m);
 }
 
-fm_status fm_attn_fwd_varlen(const void* q, const void* k, const void* v, int64_t total_tokens,
-                             int n_heads_q, int n_heads_kv, int head_dim,
-                             const int32_t* cu_seqlens, int n_seqs,
-                             const int32_t* startend_row_indices, int n_mask_heads,
-                             const int32_t* block_minmax, int causal, float softmax_scale,
-                             int block_m, int block_n, void* out, float* lse,
-                             int64_t* block_class_counts, void* workspace,
-                             size_t workspace_bytes, uint32_t flags, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Frequencies theta^(-2i/D) as double-float pairs (hi + lo).
+void rope_freqs(double theta, int head_dim, fm::RopeFreqs* fr) {
+  std::memset(fr, 0, sizeof(*fr));
+  for (int i = 0; i < head_dim / 2; ++i) {
+    const double f = std::pow(theta, -2.0 * i / head_dim);
+    fr->hi[i] = static_cast<float>(f);
+    fr->lo[i] = static_cast<float>(f - static_cast<double>(fr->hi[i]));
+  }
+}
+
+// fm_attn_fwd_varlen and fm_attn_fwd_varlen_rope: validation, tensor maps,
+// parameters and launches.  With `theta` > 0 the keys are rotated in place
+// first and every Q tile is rotated in shared memory after its load.
+fm_status attn_fwd_impl(const void* q, void* k_rot_in_place, const void* k, const void* v,
+                        int64_t total_tokens, int n_heads_q, int n_heads_kv, int head_dim,
+                        const int32_t* cu_seqlens, int n_seqs,
+                        const int32_t* startend_row_indices, int n_mask_heads,
+                        const int32_t* block_minmax, int causal, float softmax_scale,
+                        int block_m, int block_n, double theta, void* out, float* lse,
+                        void* q_rot, int64_t* block_class_counts, void* workspace,
+                        size_t workspace_bytes, uint32_t flags, void* stream) {
+  const bool fused_rope = theta != 0.0;
+  if (fused_rope && (!(theta > 0.0) || !std::isfinite(theta))) return FM_ERR_INVALID_ARG;
+  if (fused_rope && (k_rot_in_place == nullptr || k_rot_in_place != k)) return FM_ERR_INVALID_ARG;
+  if (!fused_rope && q_rot != nullptr) return FM_ERR_INVALID_ARG;
+  if (q_rot != nullptr && !aligned(q_rot, 16)) return FM_ERR_ALIGNMENT;
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || lse == nullptr ||
       cu_seqlens == nullptr || workspace == nullptr)
     return FM_ERR_INVALID_ARG;
@@ -255,7 +279,52 @@ fm_status fm_attn_fwd_varlen(const void* q, const void* k, const void* v, int64_
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t clear = sizeof(fm::AttnWorkspaceHeader) + fm::kCostBins * sizeof(int);
   if (cudaMemsetAsync(workspace, 0, clear, s) != cudaSuccess) return FM_ERR_CUDA;
-  return from_cuda(fm::launch_attn_fwd(p, tq, tk, tv, use64, num_sms, s));
+  if (!fused_rope) return from_cuda(fm::launch_attn_fwd(p, tq, tk, tv, use64, num_sms, s));
+
+  fm::RopeArgs ra;
+  rope_freqs(theta, head_dim, &ra.freqs);
+  ra.q_rot = q_rot;
+  // keys in place (the stand-alone RoPE kernel over the key heads only)
+  const int64_t kstride = static_cast<int64_t>(n_heads_kv) * head_dim;
+  const bool rope64 = use64 || total_tokens * (head_dim / 16) >= lim;
+  cudaError_t e = fm::launch_rope(k_rot_in_place, nullptr, total_tokens, n_heads_kv, 0, head_dim,
+                                  kstride, 0, cu_seqlens, n_seqs, ra.freqs, false, rope64,
+                                  num_sms, s);
+  if (e != cudaSuccess) return FM_ERR_CUDA;
+  return from_cuda(fm::launch_attn_fwd(p, tq, tk, tv, use64, num_sms, s, &ra));
+}
+
+}  // namespace
+
+extern "C" {
+
+fm_status fm_attn_fwd_varlen(const void* q, const void* k, const void* v, int64_t total_tokens,
+                             int n_heads_q, int n_heads_kv, int head_dim,
+                             const int32_t* cu_seqlens, int n_seqs,
+                             const int32_t* startend_row_indices, int n_mask_heads,
+                             const int32_t* block_minmax, int causal, float softmax_scale,
+                             int block_m, int block_n, void* out, float* lse,
+                             int64_t* block_class_counts, void* workspace,
+                             size_t workspace_bytes, uint32_t flags, void* stream) {
+  return attn_fwd_impl(q, nullptr, k, v, total_tokens, n_heads_q, n_heads_kv, head_dim,
+                       cu_seqlens, n_seqs, startend_row_indices, n_mask_heads, block_minmax,
+                       causal, softmax_scale, block_m, block_n, 0.0, out, lse, nullptr,
+                       block_class_counts, workspace, workspace_bytes, flags, stream);
+}
+
+fm_status fm_attn_fwd_varlen_rope(const void* q, void* k, const void* v, int64_t total_tokens,
+                                  int n_heads_q, int n_heads_kv, int head_dim,
+                                  const int32_t* cu_seqlens, int n_seqs, double theta,
+                                  const int32_t* startend_row_indices, int n_mask_heads,
+                                  const int32_t* block_minmax, int causal, float softmax_scale,
+                                  int block_m, int block_n, void* out, float* lse, void* q_rot,
+                                  int64_t* block_class_counts, void* workspace,
+                                  size_t workspace_bytes, uint32_t flags, void* stream) {
+  if (!(theta > 0.0) || !std::isfinite(theta) || k == nullptr) return FM_ERR_INVALID_ARG;
+  return attn_fwd_impl(q, k, k, v, total_tokens, n_heads_q, n_heads_kv, head_dim, cu_seqlens,
+                       n_seqs, startend_row_indices, n_mask_heads, block_minmax, causal,
+                       softmax_scale, block_m, block_n, theta, out, lse, q_rot,
+                       block_class_counts, workspace, workspace_bytes, flags, stream);
 }
 
 size_t fm_attn_bwd_workspace_size(int64_t total_tokens, int n_seqs, int n_heads_q) {

@@ -18,9 +18,16 @@ struct RopeFreqs {
   float lo[kMaxHalfDim];
 };
 
+// Fused Q rotation of the attention forward pass: frequencies and the
+// optional output of the rotated q ([T][Hq][D] bf16, may be q itself).
+struct RopeArgs {
+  RopeFreqs freqs;
+  void* q_rot;
+};
+
 cudaError_t launch_rope(void* q, void* k, int64_t T, int hq, int hkv, int head_dim,
                         int64_t q_stride, int64_t k_stride, const int32_t* cu, int n_seqs,
-                        const RopeFreqs& freqs, bool backward, bool use_int64,
+                        const RopeFreqs& freqs, bool backward, bool use_int64, int num_sms,
                         cudaStream_t stream);
 
 cudaError_t launch_mask_minmax(const int32_t* sri, int n_mask_heads, int64_t T,
@@ -73,9 +80,11 @@ struct AttnParams {
 
 size_t attn_workspace_bytes(int64_t T, int n_seqs, int block_m);
 
+// rope == nullptr: q is already rotated; otherwise every Q tile is rotated
+// in shared memory after its load (positions restart at each sample start).
 cudaError_t launch_attn_fwd(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, bool use_int64, int num_sms,
-                            cudaStream_t stream);
+                            cudaStream_t stream, const RopeArgs* rope = nullptr);
 
 cudaError_t launch_bounded_wait_probe(int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 

@@ -100,4 +100,15 @@ def test_validation_rejects_before_any_launch(fm):
     assert attn(ws_bytes=16) == 4
     assert attn(ws=ctypes.c_void_p(0x10010)) == 3
     assert attn(out=ctypes.c_void_p(0x10008)) == 3
+    # fused RoPE attention: theta, k, q_rot alignment, then the same checks
+    def attn_rope(theta=1e4, k=fake, q_rot=None, hq=4, hkv=2):
+        return lib.fm_attn_fwd_varlen_rope(fake, k, fake, 256, hq, hkv, 128, fake, 2, theta,
+                                           None, 0, None, 1, 0.0, 128, 128, fake, fake, q_rot,
+                                           None, fake, 1 << 20, 0, None)
+    assert attn_rope(theta=0.0) == 1
+    assert attn_rope(theta=-5.0) == 1
+    assert attn_rope(theta=float("inf")) == 1
+    assert attn_rope(k=None) == 1
+    assert attn_rope(q_rot=ctypes.c_void_p(0x10008)) == 3
+    assert attn_rope(hq=3) == 1
     assert lib.fm_debug_bounded_wait(fake, 0, None) == 1
