@@ -206,8 +206,19 @@ __device__ __forceinline__ int kv_tiles_to_scan(const AttnParams& p, int a, int 
 // planner: work unit = (sample, pair of consecutive Q tiles)
 // ---------------------------------------------------------------------------
 
+// The planner is two programmatic dependent launches (see launch_pdl): each
+// waits for the kernel before it, then lets the next one start launching,
+// so the attention kernel's set-up overlaps the planner.  Neither needs the
+// workspace cleared: the cost kernel writes every slot, the order kernel
+// builds its histogram on chip and initialises the whole header.
+
+// One warp per slot: cost = number of blocks that are not fully masked,
+// stored as cost * 2 + (the pair has a second Q tile), or -1 for a slot
+// without a Q tile.
 template <int BN, int QT>
 __global__ void __launch_bounds__(256) plan_cost_kernel(const AttnParams p) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t u = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (u >= p.n_qslots) return;
@@ -239,21 +250,39 @@ __global__ void __launch_bounds__(256) plan_cost_kernel(const AttnParams p) {
     cost += __popc(__ballot_sync(0xffffffffu, c1 != kClsF));
   }
   if (lane == 0) {
-    p.cost[u] = cost;
+    p.cost[u] = cost * 2 + (r2 > r1 ? 1 : 0);
     p.slot_info[u] = make_int2(s, static_cast<int>(pair));
-    atomicAdd(p.hist + min(cost, kCostBins - 1), 1);
-    atomicAdd(&p.ws->n_qtiles, r2 > r1 ? 2 : 1);
   }
 }
 
+// One CTA: counting sort of the real slots by cost, largest first, and the
+// workspace header (item counts, work counter, error word, timeout record).
 __global__ void __launch_bounds__(kCostBins) plan_order_kernel(const AttnParams p) {
+  __shared__ int hist[kCostBins];
   __shared__ int offs[kCostBins];
   __shared__ int warp_tot[kCostBins / 32];
+  __shared__ int n_tiles;
+  pdl_trigger();
+  pdl_wait();
   const int tid = threadIdx.x;
   const int lane = tid & 31, w = tid >> 5;
+  hist[tid] = 0;
+  if (tid == 0) n_tiles = 0;
+  __syncthreads();
+  int my_tiles = 0;
+  for (int64_t u = tid; u < p.n_qslots; u += kCostBins) {
+    const int c = p.cost[u];
+    if (c >= 0) {
+      atomicAdd(&hist[min(c >> 1, kCostBins - 1)], 1);
+      my_tiles += 1 + (c & 1);
+    }
+  }
+  my_tiles = __reduce_add_sync(0xffffffffu, my_tiles);
+  if (lane == 0 && my_tiles != 0) atomicAdd(&n_tiles, my_tiles);
+  __syncthreads();
   // descending cost: position 0 holds the largest bin
   const int bin = kCostBins - 1 - tid;
-  const int cnt = p.hist[bin];
+  const int cnt = hist[bin];
   int x = cnt;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
@@ -274,15 +303,11 @@ __global__ void __launch_bounds__(kCostBins) plan_order_kernel(const AttnParams 
   __syncthreads();
   const int incl = x + (w > 0 ? warp_tot[w - 1] : 0);
   offs[bin] = incl - cnt;
-  if (tid == kCostBins - 1) {
-    p.ws->n_items = incl * p.hq;
-    p.ws->n_tile_items = p.ws->n_qtiles * p.hq;
-  }
   __syncthreads();
   for (int64_t u = tid; u < p.n_qslots; u += kCostBins) {
     const int c = p.cost[u];
     if (c >= 0) {
-      const int pos = atomicAdd(&offs[min(c, kCostBins - 1)], 1);
+      const int pos = atomicAdd(&offs[min(c >> 1, kCostBins - 1)], 1);
       p.order[pos] = p.slot_info[u];
     }
   }
@@ -293,7 +318,17 @@ __global__ void __launch_bounds__(kCostBins) plan_order_kernel(const AttnParams 
     if (b < a || a < 0 || b > p.T) bad = true;
   }
   if (tid == 0 && (__ldg(p.cu) != 0 || __ldg(p.cu + p.n_seqs) != p.T)) bad = true;
-  if (bad) atomicOr(&p.ws->error_word, static_cast<int>(FM_DEVERR_DATA));
+  bad = __syncthreads_or(bad) != 0;
+  if (tid == kCostBins - 1) {
+    AttnWorkspaceHeader* hd = p.ws;
+    hd->work_counter = 0u;
+    hd->n_qtiles = n_tiles;
+    hd->n_items = incl * p.hq;
+    hd->n_tile_items = n_tiles * p.hq;
+    hd->error_word = bad ? static_cast<int>(FM_DEVERR_DATA) : 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) hd->diag[i] = 0;
+  }
 }
 
 // Masks columns [J0, J1) of an S row (mode 1: element bits, mode 2: columns
@@ -412,6 +447,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the planner's tables and header (and q, k, v) are ready
 
   if (warp == 0) {
     // --------------------------------------------------- K producer + metadata
@@ -1098,6 +1134,7 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p, const Rop
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
   {
     // ------------------------------------------------------------------ softmax
     const int wg = (warp - kFirstSoftmaxWarp) >> 2;  // which Q tile of the item
@@ -1485,16 +1522,15 @@ cudaError_t launch_typed(const AttnParams& p, const CUtensorMap& tq, const CUten
     if (dev < 64) configured |= 1ull << dev;
   }
   const int64_t n_slots = p.n_qslots;
-  plan_cost_kernel<BN, QT><<<static_cast<unsigned>((n_slots + 7) / 8), 256, 0, stream>>>(p);
-  e = cudaGetLastError();
+  e = launch_pdl(plan_cost_kernel<BN, QT>, dim3(static_cast<unsigned>((n_slots + 7) / 8)),
+                 dim3(256), 0, stream, p);
   if (e != cudaSuccess) return e;
-  plan_order_kernel<<<1, kCostBins, 0, stream>>>(p);
-  e = cudaGetLastError();
+  e = launch_pdl(plan_order_kernel, dim3(1), dim3(kCostBins), 0, stream, p);
   if (e != cudaSuccess) return e;
   const int64_t max_items = n_slots * p.hq;
   const int grid = static_cast<int>(max_items < num_sms ? max_items : num_sms);
-  attn_fwd_kernel<D, BN, QT, IdxT, ROPE><<<grid, kThreads<QT>, L::kBytes, stream>>>(p, tq, tk, tv, ra);
-  return cudaGetLastError();
+  return launch_pdl(attn_fwd_kernel<D, BN, QT, IdxT, ROPE>, dim3(grid), dim3(kThreads<QT>),
+                    L::kBytes, stream, p, tq, tk, tv, ra);
 }
 
 }  // namespace

@@ -251,7 +251,6 @@ fm_status attn_fwd_impl(const void* q, void* k_rot_in_place, const void* k, cons
   p.minmax = block_minmax;
   p.class_counts = block_class_counts;
   p.ws = reinterpret_cast<fm::AttnWorkspaceHeader*>(ws);
-  p.hist = reinterpret_cast<int*>(ws + sizeof(fm::AttnWorkspaceHeader));
   uint8_t* tail = ws + sizeof(fm::AttnWorkspaceHeader) + fm::kCostBins * sizeof(int);
   p.slot_info = reinterpret_cast<int2*>(tail);
   p.order = reinterpret_cast<int2*>(tail + n_qslots * sizeof(int2));
@@ -276,9 +275,8 @@ fm_status attn_fwd_impl(const void* q, void* k_rot_in_place, const void* k, cons
                      total_tokens * n_heads_q * head_dim >= lim ||
                      total_tokens * n_heads_kv * head_dim >= lim;
 
+  // (the planner initialises the workspace header itself: no memset)
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t clear = sizeof(fm::AttnWorkspaceHeader) + fm::kCostBins * sizeof(int);
-  if (cudaMemsetAsync(workspace, 0, clear, s) != cudaSuccess) return FM_ERR_CUDA;
   if (!fused_rope) return from_cuda(fm::launch_attn_fwd(p, tq, tk, tv, use64, num_sms, s));
 
   fm::RopeArgs ra;

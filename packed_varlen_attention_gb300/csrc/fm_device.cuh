@@ -13,6 +13,17 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may
+// start while the previous kernel on its stream is still finishing; it must
+// not touch global memory before pdl_wait(), which returns once that kernel
+// has completed and its writes are visible (at once when the launch was an
+// ordinary one).  pdl_trigger() lets the next kernel of the stream start
+// launching before this one ends.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -6,9 +6,33 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/fm.h"
 
 namespace fm {
+
+// Launches `kernel` as a programmatic dependent launch: its CTAs may be
+// scheduled while the previous kernel on `stream` finishes, so its launch
+// latency and set-up overlap that kernel's tail.  Every kernel launched this
+// way calls pdl_wait() before its first global-memory access, which keeps
+// stream order for memory; kernels that call pdl_trigger() let the next one
+// start early in turn.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 constexpr int kMaxHalfDim = 64;  // head_dim <= 128
 
@@ -65,7 +89,6 @@ struct AttnParams {
   int* cost;         // [n_qslots]
   int2* slot_info;   // [n_qslots] (sample, q tile)
   int2* order;       // [n_qslots] work order (sample, q tile)
-  int* hist;         // [kCostBins]
   int64_t T;
   int64_t n_qslots;
   int64_t n_kv_slots;

@@ -20,6 +20,8 @@ template <int BN>
 __global__ void __launch_bounds__(kThreads) mask_block_minmax_kernel(
     const int32_t* __restrict__ sri, int hm, int64_t T, const int32_t* __restrict__ cu,
     int n_seqs, int32_t* __restrict__ out, int64_t n_slots) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t warp_global = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (warp_global >= n_slots * hm) return;
@@ -85,14 +87,12 @@ cudaError_t launch_mask_minmax(const int32_t* sri, int n_mask_heads, int64_t T,
   const int64_t blocks = (warps + kWarps - 1) / kWarps;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  if (block_n == 128) {
-    mask_block_minmax_kernel<128><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-        sri, n_mask_heads, T, cu, n_seqs, out, n_slots);
-  } else {
-    mask_block_minmax_kernel<64><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-        sri, n_mask_heads, T, cu, n_seqs, out, n_slots);
-  }
-  return cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>(blocks));
+  if (block_n == 128)
+    return launch_pdl(mask_block_minmax_kernel<128>, grid, dim3(kThreads), 0, stream, sri,
+                      n_mask_heads, T, cu, n_seqs, out, n_slots);
+  return launch_pdl(mask_block_minmax_kernel<64>, grid, dim3(kThreads), 0, stream, sri,
+                    n_mask_heads, T, cu, n_seqs, out, n_slots);
 }
 
 }  // namespace fm

@@ -33,6 +33,8 @@ __global__ void __launch_bounds__(kThreads) rope_qk_varlen_kernel(
     int hkv, IdxT q_stride, IdxT k_stride, const int32_t* __restrict__ cu, int n_seqs,
     float sin_sign, int heads_per_group, const __grid_constant__ RopeFreqs freqs) {
   constexpr int kChunks = D / 16;  // 16-byte chunks per half row
+  pdl_trigger();
+  pdl_wait();
   const IdxT gid = static_cast<IdxT>(blockIdx.x) * kThreads + threadIdx.x;
   if (gid >= n_threads_x) return;
   const IdxT t = gid / kChunks;
@@ -94,11 +96,10 @@ cudaError_t launch_typed(void* q, void* k, int64_t T, int hq, int hkv, int64_t q
   const int groups = (hq + hkv + hpg - 1) / hpg;
   if (blocks_x > 0x7FFFFFFFLL || groups > 65535) return cudaErrorInvalidConfiguration;
   dim3 grid(static_cast<unsigned>(blocks_x), static_cast<unsigned>(groups));
-  rope_qk_varlen_kernel<IdxT, D><<<grid, kThreads, 0, stream>>>(
-      static_cast<__nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(k), static_cast<IdxT>(n), hq,
-      hkv, static_cast<IdxT>(q_stride), static_cast<IdxT>(k_stride), cu, n_seqs,
-      backward ? -1.0f : 1.0f, hpg, fr);
-  return cudaGetLastError();
+  return launch_pdl(rope_qk_varlen_kernel<IdxT, D>, grid, dim3(kThreads), 0, stream,
+                    static_cast<__nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(k),
+                    static_cast<IdxT>(n), hq, hkv, static_cast<IdxT>(q_stride),
+                    static_cast<IdxT>(k_stride), cu, n_seqs, backward ? -1.0f : 1.0f, hpg, fr);
 }
 
 }  // namespace
