@@ -154,7 +154,10 @@ struct Layout {
   static constexpr int kMeta = kCols + kMetaSlots * 4 * BN * 4;
   // int32 [kMetaSlots][kMaxRuns][8]: start column, LTS, LTE, UTS, UTE of each run
   static constexpr int kRuns = kMeta + kMetaSlots * static_cast<int>(sizeof(TileMeta));
-  static constexpr int kBars = kRuns + kMetaSlots * kMaxRuns * 8 * 4;
+  // epilogue staging: per softmax warp, 32 rows x 32 bf16 columns (2 KB)
+  static constexpr int kStage = kRuns + kMetaSlots * kMaxRuns * 8 * 4;
+  static constexpr int kStageBytesPerWarp = 32 * 64;
+  static constexpr int kBars = kStage + 4 * QT * kStageBytesPerWarp;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kEnd = kAbort + 4;
@@ -1153,31 +1156,79 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p, const Rop
     // Epilogue of an item: once its last PV is done, O / l -> bf16 out rows
     // (guarded: rows from e_rt1 on belong to the next sample) and lse.
     // `wait_bar` / `wait_par`: the barrier phase of that last PV.
+    // Each warp stages its 32 rows 32 columns at a time in shared memory
+    // (16-byte chunk u of row r at chunk u ^ ((r >> 1) & 3) of the row's 64
+    // bytes: conflict-free both ways) and stores them 8 rows per instruction,
+    // 64 contiguous bytes per row, instead of one 16-byte piece of 32
+    // different rows per instruction.
     auto epilogue = [&](int e_r, int e_rt1, int e_h, float e_m, float e_l, int wait_bar,
                         uint32_t wait_par) -> bool {
       if (!sy.warp(wait_bar, wait_par)) return false;
       tc_fence_after();
+      const uint32_t stage =
+          smem_u32(smem + L::kStage) +
+          static_cast<uint32_t>(((threadIdx.x >> 5) - kFirstSoftmaxWarp) * L::kStageBytesPerWarp);
       const float inv_l = (e_l > 0.f) ? 1.f / e_l : 0.f;
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
-                           (static_cast<IdxT>(e_r) * p.hq + e_h) * static_cast<IdxT>(D);
+      if constexpr (sizeof(IdxT) == 8) {
+        // 64-bit indexing: each thread stores its own row (the staged
+        // variant below costs this instantiation registers in the S loop)
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
+                             (static_cast<IdxT>(e_r) * p.hq + e_h) * static_cast<IdxT>(D);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(o_tmem + c * 32, rr);
-        if (e_r < e_rt1) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(o_tmem + c * 32, rr);
+          if (e_r < e_rt1) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              d4[u] = make_uint4(
+                  pack_bf16x2(__uint_as_float(rr[8 * u + 0]) * inv_l,
+                              __uint_as_float(rr[8 * u + 1]) * inv_l),
+                  pack_bf16x2(__uint_as_float(rr[8 * u + 2]) * inv_l,
+                              __uint_as_float(rr[8 * u + 3]) * inv_l),
+                  pack_bf16x2(__uint_as_float(rr[8 * u + 4]) * inv_l,
+                              __uint_as_float(rr[8 * u + 5]) * inv_l),
+                  pack_bf16x2(__uint_as_float(rr[8 * u + 6]) * inv_l,
+                              __uint_as_float(rr[8 * u + 7]) * inv_l));
+            }
+          }
+        }
+      } else {
+        const int tok0 = e_r - lane;  // token of this warp's first row
+        // rows of this warp: one 64-bit base, 32-bit offsets (32 * Hq * D fits)
+        __nv_bfloat16* const dst0 = static_cast<__nv_bfloat16*>(p.out) +
+                                    (static_cast<IdxT>(tok0) * p.hq + e_h) * static_cast<IdxT>(D);
+        const int row_elems = p.hq * D;
+        const uint32_t my_row = stage + static_cast<uint32_t>(lane) * 64u;
+        const uint32_t my_sw = static_cast<uint32_t>((lane >> 1) & 3);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(o_tmem + c * 32, rr);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            d4[u] = make_uint4(
-                pack_bf16x2(__uint_as_float(rr[8 * u + 0]) * inv_l,
-                            __uint_as_float(rr[8 * u + 1]) * inv_l),
-                pack_bf16x2(__uint_as_float(rr[8 * u + 2]) * inv_l,
-                            __uint_as_float(rr[8 * u + 3]) * inv_l),
-                pack_bf16x2(__uint_as_float(rr[8 * u + 4]) * inv_l,
-                            __uint_as_float(rr[8 * u + 5]) * inv_l),
-                pack_bf16x2(__uint_as_float(rr[8 * u + 6]) * inv_l,
-                            __uint_as_float(rr[8 * u + 7]) * inv_l));
+            st_shared_v4(my_row + ((static_cast<uint32_t>(u) ^ my_sw) << 4),
+                         pack_bf16x2(__uint_as_float(rr[8 * u + 0]) * inv_l,
+                                     __uint_as_float(rr[8 * u + 1]) * inv_l),
+                         pack_bf16x2(__uint_as_float(rr[8 * u + 2]) * inv_l,
+                                     __uint_as_float(rr[8 * u + 3]) * inv_l),
+                         pack_bf16x2(__uint_as_float(rr[8 * u + 4]) * inv_l,
+                                     __uint_as_float(rr[8 * u + 5]) * inv_l),
+                         pack_bf16x2(__uint_as_float(rr[8 * u + 6]) * inv_l,
+                                     __uint_as_float(rr[8 * u + 7]) * inv_l));
           }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int rl = 8 * i + (lane >> 2);  // row within the warp's 32
+            const uint32_t u = static_cast<uint32_t>(lane & 3);
+            const uint4 v = ld_shared_v4(stage + static_cast<uint32_t>(rl) * 64u +
+                                         ((u ^ static_cast<uint32_t>((rl >> 1) & 3)) << 4));
+            if (tok0 + rl < e_rt1)
+              *reinterpret_cast<uint4*>(dst0 + (rl * row_elems + c * 32 + static_cast<int>(u) * 8)) = v;
+          }
+          __syncwarp();
         }
       }
       if (e_r < e_rt1) {
