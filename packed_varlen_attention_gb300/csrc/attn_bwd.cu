@@ -288,6 +288,8 @@ __device__ __forceinline__ void umma_ts_group4_split(uint32_t d_tmem, uint32_t a
 template <int D, typename IdxT>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const AttnBwdParams p) {
   constexpr int G = D / 8;
+  pdl_trigger();
+  pdl_wait();
   const int64_t n_rows = p.T * p.hq;
   const int64_t r = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) / G;
   const int part = threadIdx.x % G;
@@ -337,6 +339,8 @@ __global__ void __launch_bounds__(kCostBins) bwd_plan_order_kernel(const AttnBwd
   __shared__ int warp_tot[kCostBins / 32];
   const int T = static_cast<int>(p.T);
   int* order = Mode == kModeDQ ? p.order_q : p.order_kv;
+  pdl_trigger();
+  pdl_wait();
   const int tid = threadIdx.x;
   const int lane = tid & 31, w = tid >> 5;
   tiles_in_bin[tid] = 0;
@@ -375,8 +379,18 @@ __global__ void __launch_bounds__(kCostBins) bwd_plan_order_kernel(const AttnBwd
   const int incl = x + (w > 0 ? warp_tot[w - 1] : 0);
   tiles_in_bin[bin] = incl - cnt;  // now the bin's next free position
   if (tid == kCostBins - 1) {
-    if (Mode == kModeDQ) p.ws->bwd_q_tiles = incl;
-    else p.ws->bwd_kv_tiles = incl;
+    // the header needs no clearing by the caller: this planner initialises
+    // its pass's counter (and, before the first pass, the error record)
+    if (Mode == kModeDQ) {
+      p.ws->bwd_q_tiles = incl;
+      p.ws->work_counter = 0u;
+    } else {
+      p.ws->bwd_kv_tiles = incl;
+      p.ws->work_counter_kv = 0u;
+      p.ws->error_word = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) p.ws->diag[i] = 0;
+    }
   }
   __syncthreads();
   for (int s = tid; s < p.n_seqs; s += kCostBins) {
@@ -475,6 +489,7 @@ __device__ __forceinline__ void bwd_producer_roles(const AttnBwdParams& p, const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // previous kernels' outputs (planner tables, -lse, -delta) are ready
 
   if (warp == 0) {
     // ------------------------------------------------- producer + metadata
@@ -873,6 +888,7 @@ __device__ __forceinline__ void bwd_elementwise_role(const AttnBwdParams& p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
   const int wg = (warp - 4) >> 2;  // which 32 streamed columns
   const int row = (warp & 3) * 32 + lane;
   const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -1093,13 +1109,12 @@ cudaError_t launch_mode(const AttnBwdParams& p, const CUtensorMap& tr1, const CU
     if (e != cudaSuccess) return e;
     if (dev < 64) configured |= 1ull << dev;
   }
-  bwd_plan_order_kernel<Mode><<<1, kCostBins, 0, stream>>>(p);
-  e = cudaGetLastError();
+  e = launch_pdl(bwd_plan_order_kernel<Mode>, dim3(1), dim3(kCostBins), 0, stream, p);
   if (e != cudaSuccess) return e;
   const int64_t items = p.n_res_slots * (Mode == kModeDQ ? p.hq : p.hkv);
   const int grid = static_cast<int>(items < num_sms ? items : num_sms);
-  attn_bwd_kernel<D, Mode, IdxT><<<grid, kBwdThreads, L::kBytes, stream>>>(p, tr1, tr2, tc1, tc2);
-  return cudaGetLastError();
+  return launch_pdl(attn_bwd_kernel<D, Mode, IdxT>, dim3(grid), dim3(kBwdThreads), L::kBytes,
+                    stream, p, tr1, tr2, tc1, tc2);
 }
 
 template <int D, typename IdxT>
@@ -1107,8 +1122,8 @@ cudaError_t launch_all(const AttnBwdParams& p, const BwdMaps& m, int num_sms,
                        cudaStream_t stream) {
   const int64_t rows = p.T * p.hq;
   const int64_t blocks = (rows * (D / 8) + 255) / 256;
-  bwd_prep_kernel<D, IdxT><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(bwd_prep_kernel<D, IdxT>, dim3(static_cast<unsigned>(blocks)),
+                             dim3(256), 0, stream, p);
   if (e != cudaSuccess) return e;
   e = launch_mode<D, kModeDKV, IdxT>(p, m.k128, m.v128, m.q64, m.do64, num_sms, stream);
   if (e != cudaSuccess) return e;
@@ -1117,7 +1132,7 @@ cudaError_t launch_all(const AttnBwdParams& p, const BwdMaps& m, int num_sms,
 
 }  // namespace
 
-// Workspace: header (cleared per call) | order_q | order_kv (n_slots ints
+// Workspace: header (initialised by the planners) | order_q | order_kv (n_slots ints
 // each) | -lse*log2(e) | -delta ([Hq][T] floats each).
 size_t attn_bwd_clear_bytes() { return sizeof(AttnWorkspaceHeader); }
 

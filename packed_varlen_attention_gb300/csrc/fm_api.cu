@@ -411,9 +411,8 @@ fm_status fm_attn_bwd_varlen(const void* q, const void* k, const void* v, const 
                      total_tokens * n_heads_q * head_dim >= lim ||
                      total_tokens * n_heads_kv * head_dim >= lim;
 
+  // (the backward planners initialise the workspace header: no memset)
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, fm::attn_bwd_clear_bytes(), s) != cudaSuccess)
-    return FM_ERR_CUDA;
   return from_cuda(fm::launch_attn_bwd(p, m, use64, num_sms, s));
 }
 
