@@ -117,6 +117,18 @@ def effective_flops(wl) -> float:
                                    for h in range(wl.n_heads_q))
 
 
+def tile_accounting(wl, counts, attn_ms):
+    """Work the kernel executes: every block that is not fully masked runs
+    full block_m x block_n MMAs (partially masked ones included), 4 * D
+    FLOPs per (query, key) pair of the block; tile efficiency = effective /
+    executed."""
+    executed = 4.0 * wl.head_dim * wl.block_m * wl.block_n * (counts[1] + counts[2])
+    eff = effective_flops(wl)
+    return {"executed_tflop_per_call": executed / 1e12,
+            "executed_tflops": executed / (attn_ms * 1e-3) / 1e12,
+            "tile_efficiency": eff / executed if executed > 0 else None}
+
+
 def rope_bytes(wl) -> float:
     return 2.0 * wl.total_tokens * (wl.n_heads_q + wl.n_heads_kv) * wl.head_dim * 2
 
@@ -344,7 +356,17 @@ def time_config(fm, torch, batch, steps, warmup, flush, peaks):
     rope = [e[0].elapsed_time(e[1]) for e in evs]
     mm = [e[1].elapsed_time(e[2]) for e in evs]
     attn = [e[2].elapsed_time(e[3]) for e in evs]
-    tot = [e[0].elapsed_time(e[3]) for e in evs]
+    # whole steps with events only at their ends (no cut between the calls)
+    ends = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(steps)]
+    for i in range(steps):
+        batch.restore()
+        flush()
+        ends[i][0].record()
+        batch.step(fm)
+        ends[i][1].record()
+    torch.cuda.synchronize()
+    tot = [a.elapsed_time(e) for a, e in ends]
     return {"rope_ms": float(np.mean(rope)), "minmax_ms": float(np.mean(mm)),
             "attn_ms": float(np.mean(attn)), "step_ms": float(np.mean(tot)),
             "step_ms_sum": float(np.sum(tot))}
@@ -442,6 +464,7 @@ def run_ours(args):
             "effective_tflop_per_step": fl / 1e12,
             "block_counts_fpu": counts.cpu().tolist(),
             "tokens": wl.total_tokens,
+            **tile_accounting(wl, counts.cpu().tolist(), t["attn_ms"]),
         }
         per_config[gen.CONFIG_NAMES[cfg]]["fused_rope"] = fused_entry(
             fl, time_fused(fm, torch, b, max(5, min(args.steps, 20)), 3, flush), t["step_ms"])
@@ -474,14 +497,26 @@ def run_ours(args):
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
+    # the timed steps carry events only at their ends (events between the
+    # calls would cut the overlap of the programmatic dependent launches)
+    step_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+    for i in range(args.steps):
+        b.restore()
+        flush()
+        step_evs[i][0].record()
+        b.step(fm)
+        step_evs[i][1].record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    # per-call breakdown from as many further steps with events between the calls
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     for i in range(args.steps):
         b.restore()
         flush()
         b.step(fm, events=evs[i])
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
     torch.cuda.synchronize()
     # e2e: same step through pinned host buffers, copies inside the timed region
     e2e_start = torch.cuda.Event(enable_timing=True)
@@ -499,7 +534,7 @@ def run_ours(args):
     bwd_ms = time_backward(fm, torch, b, args.steps, max(3, args.warmup), flush)
     clocks = sampler.stop()
 
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    step_ms = [a.elapsed_time(e) for a, e in step_evs]
     attn_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
     rope_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
     mm_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
@@ -529,6 +564,7 @@ def run_ours(args):
         "minmax_us": mm_ms * 1e3, "attn_ms": attn_ms, "rope_ms": rope_ms,
         "step_ms": float(np.mean(step_ms)), "effective_tflop_per_step": fl / 1e12,
         "block_counts_fpu": counts.cpu().tolist(), "tokens": wl.total_tokens,
+        **tile_accounting(wl, counts.cpu().tolist(), attn_ms),
         "backward": backward_entry(fl, bwd_ms, peaks),
         "fused_rope": fused_entry(fl, fused_ms, float(np.mean(step_ms))),
     }
