@@ -511,6 +511,28 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    # the same step captured once in a CUDA graph and replayed (the calls are
+    # stream-ordered and allocate nothing, so a training loop can do this)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        b.restore()
+        b.step(fm)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        b.step(fm)
+    graph_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)]
+    for i in range(args.steps):
+        b.restore()
+        flush()
+        graph_evs[i][0].record()
+        graph.replay()
+        graph_evs[i][1].record()
+    torch.cuda.synchronize()
+    graph_ms = float(np.mean([a.elapsed_time(e) for a, e in graph_evs]))
     # per-call breakdown from as many further steps with events between the calls
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     for i in range(args.steps):
@@ -567,6 +589,8 @@ def run_ours(args):
         **tile_accounting(wl, counts.cpu().tolist(), attn_ms),
         "backward": backward_entry(fl, bwd_ms, peaks),
         "fused_rope": fused_entry(fl, fused_ms, float(np.mean(step_ms))),
+        "cuda_graph_step": {"ms": graph_ms, "effective_tflops": fl / (graph_ms * 1e-3) / 1e12,
+                            "note": "the same step captured once and replayed"},
     }
     line = {
         "metric": METRIC,
