@@ -315,6 +315,63 @@ class Batch:
                                 out=self.out, lse=self.lse, q_rot=self.q_rot, workspace=self.ws,
                                 force_int64=wl.force_int64)
 
+    def pipelined_e2e(self, fm, torch, steps):
+        """`steps` steps through host buffers with the copies pipelined: the
+        inputs of step i+1 go to a second set of device buffers on a copy
+        stream while step i computes, and each step's out / lse come back on a
+        third stream.  Returns the wall time of all steps (ms, CUDA events)."""
+        wl = self.wl
+        dev = self.q.device
+        sets = [(self.q, self.k, self.v, self.cu, self.sri),
+                tuple(torch.empty_like(t) for t in (self.q, self.k, self.v, self.cu, self.sri))]
+        outs = [(self.out, self.lse), (torch.empty_like(self.out), torch.empty_like(self.lse))]
+        h2d = torch.cuda.Stream(device=dev)
+        d2h = torch.cuda.Stream(device=dev)
+        comp = torch.cuda.current_stream(dev)
+        loaded = [torch.cuda.Event() for _ in range(2)]
+        computed = [torch.cuda.Event() for _ in range(2)]
+        drained = [torch.cuda.Event() for _ in range(2)]  # an output set copied back
+        host = (self.h_q, self.h_k, self.h_v, self.h_cu, self.h_sri)
+
+        def load(i):
+            j = i % 2
+            with torch.cuda.stream(h2d):
+                if i >= 2:
+                    h2d.wait_event(computed[j])  # step i-2 is done with this input set
+                for d, h in zip(sets[j], host):
+                    d.copy_(h, non_blocking=True)
+                loaded[j].record(h2d)
+
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(comp)
+        load(0)
+        for i in range(steps):
+            j = i % 2
+            if i + 1 < steps:
+                load(i + 1)
+            comp.wait_event(loaded[j])
+            if i >= 2:
+                comp.wait_event(drained[j])  # step i-2's results left this output set
+            q, k, v, cu, sri = sets[j]
+            out, lse = outs[j]
+            fm.rope_qk_varlen(q, k, cu, wl.theta, force_int64=wl.force_int64)
+            fm.mask_block_minmax(sri, cu, wl.block_n, out=self.mm)
+            fm.attn_fwd_varlen(q, k, v, cu, sri, self.mm, causal=wl.causal, block_m=wl.block_m,
+                               block_n=wl.block_n, out=out, lse=lse, workspace=self.ws,
+                               force_int64=wl.force_int64)
+            computed[j].record(comp)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(computed[j])
+                self.h_out.copy_(out, non_blocking=True)
+                self.h_lse.copy_(lse, non_blocking=True)
+                drained[j].record(d2h)
+        comp.wait_stream(d2h)
+        t1.record(comp)
+        t1.synchronize()
+        return t0.elapsed_time(t1)
+
     def backward(self, fm):
         """Gradients of the step's attention (q, k after RoPE; out, lse of the step)."""
         wl = self.wl
@@ -551,6 +608,8 @@ def run_ours(args):
         e2e_stop.record()
         e2e_stop.synchronize()
         e2e_ms.append(e2e_start.elapsed_time(e2e_stop))
+    # e2e with the host copies pipelined against the compute (input prefetch)
+    e2e_pipe_ms = b.pipelined_e2e(fm, torch, args.steps)
     # fused-RoPE variant and backward of the same batch (outside the step's timed region)
     fused_ms = time_fused(fm, torch, b, args.steps, max(3, args.warmup), flush)
     bwd_ms = time_backward(fm, torch, b, args.steps, max(3, args.warmup), flush)
@@ -633,6 +692,12 @@ def run_ours(args):
         "rope": {"bound": "hbm", "achieved": rope_gbs, "unit": "GB/s",
                  "peak": peaks["hbm_gbs"], "frac": rope_gbs / peaks["hbm_gbs"],
                  "frac_of_8tbs": rope_gbs / 8000.0, "bytes": rb},
+        "e2e_pipelined": {
+            "value": fl * args.steps / (e2e_pipe_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": e2e_pipe_ms / args.steps,
+            "note": "same H2D / D2H bytes per step; step i+1's inputs copied on a second stream "
+                    "into a second buffer set while step i computes, results read back on a "
+                    "third stream"},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": b.h2d_bytes, "d2h_bytes_per_step": b.d2h_bytes},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
