@@ -1588,7 +1588,7 @@ cudaError_t launch_typed(const AttnParams& p, const CUtensorMap& tq, const CUten
 
 size_t attn_workspace_bytes(int64_t T, int n_seqs, int block_m) {
   const int64_t n_qslots = T / block_m + n_seqs;
-  size_t bytes = sizeof(AttnWorkspaceHeader) + kCostBins * sizeof(int);
+  size_t bytes = sizeof(AttnWorkspaceHeader);
   bytes += static_cast<size_t>(n_qslots) * (sizeof(int) + 2 * sizeof(int2));
   return (bytes + 255) & ~static_cast<size_t>(255);
 }

@@ -12,8 +12,8 @@
 // caller lives here in one file-scope __device__ array of kScratchBytes bytes.
 // Every GPU that loads this library holds that array until the process exits.
 // The array is shared by every call on a device and keeps the last call's
-// contents; each call first clears the part that must start at zero (work
-// counter, error word, cost histogram), exactly as with a caller workspace.
+// contents; each call's planner first initialises the part that must start
+// at zero (work counter, error word), exactly as with a caller workspace.
 // Calls that overlap on the GPU (different streams without ordering) race
 // on the array and give wrong results: order them on one stream.
 #include <mutex>
@@ -25,10 +25,9 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 // Up to 32768 Q-tile slots (floor(T / block_m) + n_seqs), e.g. 4M tokens at
-// block_m = 128: 256-byte header, 1024-bin histogram, 20 bytes per slot.
+// block_m = 128: 256-byte header, 20 bytes per slot.
 constexpr int64_t kMaxQSlots = 32768;
-constexpr size_t kScratchBytes =
-    sizeof(fm::AttnWorkspaceHeader) + fm::kCostBins * sizeof(int) + kMaxQSlots * 20;
+constexpr size_t kScratchBytes = sizeof(fm::AttnWorkspaceHeader) + kMaxQSlots * 20;
 static_assert(kScratchBytes % 256 == 0, "scratch size is a multiple of 256 bytes");
 
 }  // namespace

@@ -251,7 +251,7 @@ fm_status attn_fwd_impl(const void* q, void* k_rot_in_place, const void* k, cons
   p.minmax = block_minmax;
   p.class_counts = block_class_counts;
   p.ws = reinterpret_cast<fm::AttnWorkspaceHeader*>(ws);
-  uint8_t* tail = ws + sizeof(fm::AttnWorkspaceHeader) + fm::kCostBins * sizeof(int);
+  uint8_t* tail = ws + sizeof(fm::AttnWorkspaceHeader);
   p.slot_info = reinterpret_cast<int2*>(tail);
   p.order = reinterpret_cast<int2*>(tail + n_qslots * sizeof(int2));
   p.cost = reinterpret_cast<int*>(tail + 2 * n_qslots * sizeof(int2));
