@@ -217,3 +217,16 @@ def test_fused_headline_sampled_against_oracle(fm):
     heads = [0, 9, 31]
     _compare(b, oracle_fused(wl, rows=rows, heads=heads), rows=rows, heads=heads,
              what="cfg2 fused")
+
+
+@pytest.mark.parametrize("seed", range(2))
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("per_head", [False, True])
+@pytest.mark.parametrize("block_n", [128, 64])
+def test_fused_equals_unfused_random_intervals(fm, seed, causal, per_head, block_n):
+    """Arbitrary column intervals (many partially masked blocks, rows with no
+    visible key), one mask shared by all heads or one mask per q head."""
+    wl = gen.make_custom([3, 200, 129, 0, 64, 400], n_heads_q=4, n_heads_kv=1, head_dim=128,
+                         mask="random", causal=causal, seed=seed, theta=1.0e4,
+                         n_mask_heads=4 if per_head else 1)
+    assert_bitwise(fm, wl, 128, block_n, causal)
