@@ -222,6 +222,21 @@ def measured_traffic():
         return None
 
 
+def replica_throughput(torch, world, flop_per_step, steps, ms_totals, device="cpu"):
+    """Whole-job throughput of `world` replicas (TFLOP/s): every rank did
+    `steps` steps of `flop_per_step` each; the job took as long as its slowest
+    rank, so each timed total (ms) is max-reduced over the ranks first (a
+    collective over the default process group when world > 1).  Returns
+    (throughputs, max-reduced totals), one per entry of `ms_totals`."""
+    totals = [float(x) for x in ms_totals]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor(totals, dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        totals = [float(x) for x in t.tolist()]
+    return [world * flop_per_step * steps / (ms * 1e-3) / 1e12 for ms in totals], totals
+
+
 def dist_info():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -619,15 +634,8 @@ def run_ours(args):
     attn_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
     rope_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
     mm_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
-    total_ms = float(np.sum(step_ms))
-    e2e_total = float(np.sum(e2e_ms))
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms, e2e_total], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_total = float(t[0]), float(t[1])
-    value = world * fl * args.steps / (total_ms * 1e-3) / 1e12
-    e2e_value = world * fl * args.steps / (e2e_total * 1e-3) / 1e12
+    (value, e2e_value), (total_ms, e2e_total) = replica_throughput(
+        torch, world, fl, args.steps, [np.sum(step_ms), np.sum(e2e_ms)], device)
     attn_tflops = fl / (attn_ms * 1e-3) / 1e12
     rb = rope_bytes(wl)
     rope_gbs = rb / (rope_ms * 1e-3) / 1e9
