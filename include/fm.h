@@ -9,7 +9,12 @@
  * (except fm_get_device_error, which reads one word back) and keeps no
  * state beyond cached device attributes and resolved driver entry points.
  * `stream` is a cudaStream_t passed as void*; NULL is the legacy default
- * stream.  All kernels are enqueued on `stream` in call order.
+ * stream.  All kernels are enqueued on `stream` in call order, as
+ * programmatic dependent launches: a kernel may begin its set-up while the
+ * previous kernel on the stream finishes, and touches no global memory
+ * before that kernel has completed, so stream order holds for every buffer.
+ * The calls may be captured in a CUDA graph; make the first call on a device
+ * outside capture (it caches device attributes and sets kernel attributes).
  *
  * Packed layout (Unsloth packing blog, section "Why padding is needed";
  * Varlen-Packing technical document, section 1.1): documents are
