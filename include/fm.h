@@ -101,6 +101,24 @@ FM_API fm_status fm_rope_qk_varlen(void* q, void* k, int64_t total_tokens, int n
                             double theta, int backward, uint32_t flags, void* stream);
 
 /*
+ * fm_rope_index_bits / fm_attn_index_bits -- the index width (32 or 64) that
+ * fm_rope_qk_varlen / the attention calls (forward, fused-RoPE forward,
+ * backward) choose for these sizes; -1 on negative sizes.
+ *
+ * Unsloth packing blog, section "Int64 indexing for Triton kernels": 32-bit
+ * offsets overflow at long contexts, while always-64-bit indexing slows
+ * training slightly, so the width is a compile-time specialisation chosen
+ * per call.  Offsets are 32-bit unless an element offset can reach 2^31
+ * (RoPE: T * token stride of q or k, or T * head_dim / 16 threads;
+ * attention: T * Hq * D or T * Hkv * D), or FM_FLAG_FORCE_INT64 asks for
+ * 64-bit; both widths give identical results.
+ */
+FM_API int fm_rope_index_bits(int64_t total_tokens, int n_heads_kv, int head_dim,
+                              int64_t q_token_stride, int64_t k_token_stride, uint32_t flags);
+FM_API int fm_attn_index_bits(int64_t total_tokens, int n_heads_q, int n_heads_kv, int head_dim,
+                              uint32_t flags);
+
+/*
  * fm_num_kv_tiles_bound -- number of per-tile slots used by the block
  * statistics layout below: floor(T / block_n) + n_seqs.
  *

@@ -27,6 +27,8 @@ __all__ = [
     "FMError",
     "rope_qk_varlen",
     "num_kv_tiles_bound",
+    "rope_index_bits",
+    "attn_index_bits",
     "mask_block_minmax",
     "attn_fwd_workspace_size",
     "attn_fwd_varlen",
@@ -61,6 +63,8 @@ _SIGNATURES = {
     "fm_rope_qk_varlen": (_c_int, [_c_vp, _c_vp, _c_i64, _c_int, _c_int, _c_int, _c_i64, _c_i64,
                                    _c_vp, _c_int, ctypes.c_double, _c_int, _c_u32, _c_vp]),
     "fm_num_kv_tiles_bound": (_c_i64, [_c_i64, _c_int, _c_int]),
+    "fm_rope_index_bits": (_c_int, [_c_i64, _c_int, _c_int, _c_i64, _c_i64, _c_u32]),
+    "fm_attn_index_bits": (_c_int, [_c_i64, _c_int, _c_int, _c_int, _c_u32]),
     "fm_mask_block_minmax": (_c_int, [_c_vp, _c_int, _c_i64, _c_vp, _c_int, _c_int, _c_vp,
                                       _c_i64, _c_vp]),
     "fm_attn_fwd_workspace_size": (ctypes.c_size_t, [_c_i64, _c_int, _c_int, _c_int]),
@@ -165,6 +169,20 @@ def rope_qk_varlen(q: torch.Tensor, k: Optional[torch.Tensor], cu_seqlens: torch
         _ptr(q), _ptr(k), T, hq, hkv, d, q.stride(0), ks, _ptr(cu_seqlens),
         cu_seqlens.numel() - 1, float(theta), int(bool(backward)),
         FM_FLAG_FORCE_INT64 if force_int64 else 0, _stream(stream)))
+
+
+def rope_index_bits(total_tokens: int, n_heads_kv: int, head_dim: int, q_token_stride: int,
+                    k_token_stride: int, force_int64: bool = False) -> int:
+    """Index width (32 or 64) rope_qk_varlen uses for these sizes."""
+    return int(_lib().fm_rope_index_bits(total_tokens, n_heads_kv, head_dim, q_token_stride,
+                                         k_token_stride, FM_FLAG_FORCE_INT64 if force_int64 else 0))
+
+
+def attn_index_bits(total_tokens: int, n_heads_q: int, n_heads_kv: int, head_dim: int,
+                    force_int64: bool = False) -> int:
+    """Index width (32 or 64) the attention calls use for these sizes."""
+    return int(_lib().fm_attn_index_bits(total_tokens, n_heads_q, n_heads_kv, head_dim,
+                                         FM_FLAG_FORCE_INT64 if force_int64 else 0))
 
 
 def num_kv_tiles_bound(total_tokens: int, n_seqs: int, block_n: int) -> int:

@@ -130,15 +130,34 @@ fm_status fm_rope_qk_varlen(void* q, void* k, int64_t total_tokens, int n_heads_
     fr.hi[i] = static_cast<float>(f);
     fr.lo[i] = static_cast<float>(f - static_cast<double>(fr.hi[i]));
   }
-  const int64_t lim = int64_t(1) << 31;
-  bool use64 = (flags & FM_FLAG_FORCE_INT64) != 0;
-  use64 = use64 || total_tokens * q_token_stride >= lim;
-  use64 = use64 || (n_heads_kv > 0 && total_tokens * k_token_stride >= lim);
-  use64 = use64 || total_tokens * (head_dim / 16) >= lim;
+  const bool use64 = fm_rope_index_bits(total_tokens, n_heads_kv, head_dim, q_token_stride,
+                                        k_token_stride, flags) == 64;
   return from_cuda(fm::launch_rope(q, k, total_tokens, n_heads_q, n_heads_kv, head_dim,
                                    q_token_stride, k_token_stride, cu_seqlens, n_seqs, fr,
                                    backward != 0, use64, num_sms,
                                    static_cast<cudaStream_t>(stream)));
+}
+
+int fm_rope_index_bits(int64_t total_tokens, int n_heads_kv, int head_dim,
+                       int64_t q_token_stride, int64_t k_token_stride, uint32_t flags) {
+  if (total_tokens < 0 || n_heads_kv < 0 || head_dim <= 0 || q_token_stride < 0 ||
+      k_token_stride < 0)
+    return -1;
+  const int64_t lim = int64_t(1) << 31;
+  const bool use64 = (flags & FM_FLAG_FORCE_INT64) != 0 || total_tokens * q_token_stride >= lim ||
+                     (n_heads_kv > 0 && total_tokens * k_token_stride >= lim) ||
+                     total_tokens * (head_dim / 16) >= lim;
+  return use64 ? 64 : 32;
+}
+
+int fm_attn_index_bits(int64_t total_tokens, int n_heads_q, int n_heads_kv, int head_dim,
+                       uint32_t flags) {
+  if (total_tokens < 0 || n_heads_q < 0 || n_heads_kv < 0 || head_dim <= 0) return -1;
+  const int64_t lim = int64_t(1) << 31;
+  const bool use64 = (flags & FM_FLAG_FORCE_INT64) != 0 ||
+                     total_tokens * n_heads_q * head_dim >= lim ||
+                     total_tokens * n_heads_kv * head_dim >= lim;
+  return use64 ? 64 : 32;
 }
 
 int64_t fm_num_kv_tiles_bound(int64_t total_tokens, int n_seqs, int block_n) {
@@ -271,9 +290,8 @@ fm_status attn_fwd_impl(const void* q, void* k_rot_in_place, const void* k, cons
   p.timeout_ns = 1000000000ull;
 
   const int64_t lim = int64_t(1) << 31;
-  const bool use64 = (flags & FM_FLAG_FORCE_INT64) != 0 ||
-                     total_tokens * n_heads_q * head_dim >= lim ||
-                     total_tokens * n_heads_kv * head_dim >= lim;
+  const bool use64 =
+      fm_attn_index_bits(total_tokens, n_heads_q, n_heads_kv, head_dim, flags) == 64;
 
   // (the planner initialises the workspace header itself: no memset)
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -406,10 +424,8 @@ fm_status fm_attn_bwd_varlen(const void* q, const void* k, const void* v, const 
   p.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
   p.timeout_ns = 1000000000ull;
 
-  const int64_t lim = int64_t(1) << 31;
-  const bool use64 = (flags & FM_FLAG_FORCE_INT64) != 0 ||
-                     total_tokens * n_heads_q * head_dim >= lim ||
-                     total_tokens * n_heads_kv * head_dim >= lim;
+  const bool use64 =
+      fm_attn_index_bits(total_tokens, n_heads_q, n_heads_kv, head_dim, flags) == 64;
 
   // (the backward planners initialise the workspace header: no memset)
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -112,3 +112,23 @@ def test_validation_rejects_before_any_launch(fm):
     assert attn_rope(q_rot=ctypes.c_void_p(0x10008)) == 3
     assert attn_rope(hq=3) == 1
     assert lib.fm_debug_bounded_wait(fake, 0, None) == 1
+
+
+def test_index_width_switches_at_2_pow_31(fm):
+    """Int64 indexing only where an element offset can reach 2^31 (host-only:
+    the same function the calls use to pick their instantiation)."""
+    lim = 1 << 31
+    # attention: T * Hq * D or T * Hkv * D reaching 2^31
+    assert fm.attn_index_bits(lim // (32 * 128) - 1, 32, 8, 128) == 32
+    assert fm.attn_index_bits(lim // (32 * 128), 32, 8, 128) == 64
+    assert fm.attn_index_bits(lim // (8 * 128), 1, 8, 128) == 64   # via the key/value heads
+    assert fm.attn_index_bits(131072, 32, 8, 128) == 32            # 2^29: only forced
+    assert fm.attn_index_bits(131072, 32, 8, 128, force_int64=True) == 64
+    assert fm.attn_index_bits(-1, 32, 8, 128) == -1
+    # RoPE: T * token stride of q or k, or T * D / 16 threads
+    assert fm.rope_index_bits(8192, 8, 128, 32 * 128, 8 * 128) == 32
+    assert fm.rope_index_bits(lim // 4096, 8, 128, 4096, 1024) == 64
+    assert fm.rope_index_bits(lim // 4096 - 1, 8, 128, 4096, 1024) == 32
+    assert fm.rope_index_bits(lim // 1024, 8, 128, 128, 1024) == 64   # k stride
+    assert fm.rope_index_bits(lim // 1024, 0, 128, 128, 1 << 40) == 32  # no k heads
+    assert fm.rope_index_bits(8192, 8, 128, 4096, 1024, force_int64=True) == 64
