@@ -132,3 +132,21 @@ def test_index_width_switches_at_2_pow_31(fm):
     assert fm.rope_index_bits(lim // 1024, 8, 128, 128, 1024) == 64   # k stride
     assert fm.rope_index_bits(lim // 1024, 0, 128, 128, 1 << 40) == 32  # no k heads
     assert fm.rope_index_bits(8192, 8, 128, 4096, 1024, force_int64=True) == 64
+
+
+def test_header_compiles_as_c_and_links(fm, tmp_path):
+    """A plain C99 program builds against include/fm.h, links libfm.so and
+    gets the expected answers from the calls that need no GPU."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    lib_dir = os.path.dirname(fm.library_path())
+    exe = str(tmp_path / "abi_from_c")
+    src = os.path.join(ROOT, "tests", "c", "abi_from_c.c")
+    subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), src,
+                    "-o", exe, "-L", lib_dir, "-lfm", "-Wl,-rpath," + lib_dir], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == "ok FM_ERR_WORKSPACE"
