@@ -18,6 +18,7 @@ import numpy as np
 import pytest
 
 from helpers import bf16_tensor_to_f64, ensure_library, to_device_bf16
+import oracle_runs
 from oracle import attention_bwd as ob
 from workloads import gen
 
@@ -32,9 +33,7 @@ def fm():
 
 
 def _dout_bits(wl, seed):
-    rng = np.random.default_rng(1000 + seed)
-    return gen.f32_to_bf16_bits(
-        rng.standard_normal((wl.total_tokens, wl.n_heads_q, wl.head_dim)).astype(np.float32))
+    return oracle_runs.dout_bits(wl, seed)
 
 
 def run_grad(fm, wl, do_bits, causal=None, force_int64=False, sri="default"):
@@ -199,32 +198,15 @@ def test_int64_path_bit_identical(fm):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
 
 
-def _sample_rows(wl, rng, extra=1500):
-    cu = wl.cu_seqlens.astype(np.int64)
-    rows = [rng.integers(0, wl.total_tokens, extra)]
-    for s in range(wl.n_seqs):
-        a, b = int(cu[s]), int(cu[s + 1])
-        if b > a:
-            rows.append(np.arange(a, min(a + 128, b)))
-            rows.append(np.arange(max(a, b - 128), b))
-    return np.unique(np.concatenate(rows))
-
-
 @pytest.mark.parametrize("cfg", [2, 3, 4])
-def test_full_size_configs_sampled(fm, cfg):
+def test_full_size_configs(fm, cfg):
     """The full-size workloads in the launch configuration the benchmark
-    times; two key/value heads (and their q heads) against the oracle on
-    sampled rows."""
+    times: every row of every q and key/value head against the oracle."""
     wl = gen.make_workload(cfg, seed=0)
     do = _dout_bits(wl, cfg)
     got = run_grad(fm, wl, do)
-    rng = np.random.default_rng(cfg)
-    kvs = sorted({0, wl.n_heads_kv - 1})
-    ref, mags = oracle_grad(wl, do, kv_heads=kvs)
-    grp = wl.n_heads_q // wl.n_heads_kv
-    hq = [h for g in kvs for h in range(g * grp, (g + 1) * grp)]
-    rows = _sample_rows(wl, rng)
-    check_all(got, ref, mags, f"cfg{cfg}", rows=rows, heads_q=hq, heads_kv=kvs)
+    ref, mags = oracle_runs.backward_full(cfg, 0, cfg)
+    check_all(got, ref, mags, f"cfg{cfg}")
 
 
 def test_unsupported_arguments_raise(fm):

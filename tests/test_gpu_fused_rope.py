@@ -13,8 +13,9 @@ prologue) against the unfused path and against the float64 oracle.
 import numpy as np
 import pytest
 
-from helpers import (ATTN_MAX_ABS, ATTN_MEAN_ABS, bf16_tensor_to_f64, check_close_bf16, check_lse,
-                     ensure_library, to_device_bf16)
+from helpers import (ATTN_MAX_ABS, ATTN_MEAN_ABS, abs_v_magnitude, bf16_tensor_to_f64,
+                     check_close_bf16, check_lse, ensure_library, to_device_bf16, workload_inputs)
+import oracle_runs
 from oracle import attention as oat
 from oracle import rope as orope
 from workloads import gen
@@ -176,7 +177,11 @@ def oracle_fused(wl, rows=None, heads=None):
     return out, lse
 
 
-def _compare(b, ref, rows=None, heads=None, what=""):
+def _compare(b, ref, rows=None, heads=None, what="", wl=None):
+    mag = None
+    if wl is not None:
+        mag = abs_v_magnitude(workload_inputs(wl, rope=True), wl.cu_seqlens,
+                              wl.startend_row_indices, wl.causal, rows, heads)
     o = bf16_tensor_to_f64(b["out"])
     l_ = b["lse"].cpu().numpy().astype(np.float64)
     ro, rl = ref
@@ -184,14 +189,14 @@ def _compare(b, ref, rows=None, heads=None, what=""):
         o, ro, l_, rl = o[rows], ro[rows], l_[:, rows], rl[:, rows]
     if heads is not None:
         o, ro, l_, rl = o[:, heads], ro[:, heads], l_[heads], rl[heads]
-    check_close_bf16(o, ro, ATTN_MAX_ABS, ATTN_MEAN_ABS, what=what + " out")
+    check_close_bf16(o, ro, ATTN_MAX_ABS, ATTN_MEAN_ABS, what=what + " out", magnitude=mag)
     check_lse(l_, rl, what=what + " lse")
 
 
 def test_fused_tiny_against_oracle(fm):
     wl = gen.make_workload(1, seed=0)
     b = run_fused(fm, wl, wl.block_m, wl.block_n, wl.causal)
-    _compare(b, oracle_fused(wl), what="cfg1 fused")
+    _compare(b, oracle_fused(wl), what="cfg1 fused", wl=wl)
     assert b["counts"].tolist() == [2, 5, 2]
 
 
@@ -201,22 +206,16 @@ def test_fused_small_against_oracle(fm, head_dim, mask, causal):
     wl = gen.make_custom(LENS, n_heads_q=4, n_heads_kv=2, head_dim=head_dim, mask=mask,
                          causal=causal, seed=23, theta=1.0e4)
     b = run_fused(fm, wl, 128, 128, causal)
-    _compare(b, oracle_fused(wl), what=f"{mask} D{head_dim} fused")
+    _compare(b, oracle_fused(wl), what=f"{mask} D{head_dim} fused", wl=wl)
 
 
-def test_fused_headline_sampled_against_oracle(fm):
-    wl = gen.make_workload(2, seed=0)
-    b = run_fused(fm, wl, 128, 128, True)
-    rng = np.random.default_rng(42)
-    cu = wl.cu_seqlens.astype(np.int64)
-    rows = [rng.integers(0, wl.total_tokens, 1500)]
-    for s in range(wl.n_seqs):
-        a, e = int(cu[s]), int(cu[s + 1])
-        rows.append(np.arange(max(a, e - 64), e))
-    rows = np.unique(np.concatenate(rows))
-    heads = [0, 9, 31]
-    _compare(b, oracle_fused(wl, rows=rows, heads=heads), rows=rows, heads=heads,
-             what="cfg2 fused")
+@pytest.mark.parametrize("cfg", [2, 3, 4])
+def test_fused_full_size_against_oracle(fm, cfg):
+    """Workloads 2-4 in full (every row, every q head): the fused call
+    against the oracle on RoPE(q), RoPE(k) stored as bfloat16."""
+    wl = gen.make_workload(cfg, seed=0)
+    b = run_fused(fm, wl, 128, 128, wl.causal)
+    _compare(b, oracle_runs.forward_full(cfg, 0, rope=True), what=f"cfg{cfg} fused", wl=wl)
 
 
 @pytest.mark.parametrize("seed", range(2))

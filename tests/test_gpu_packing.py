@@ -12,7 +12,8 @@ samples).  The pack is also checked against the float64 oracle.
 import numpy as np
 import pytest
 
-from helpers import ATTN_MAX_ABS, ATTN_MEAN_ABS, bf16_tensor_to_f64, check_close_bf16, check_lse, ensure_library
+from helpers import (ATTN_MAX_ABS, ATTN_MEAN_ABS, abs_v_magnitude, bf16_tensor_to_f64,
+                     check_close_bf16, check_lse, ensure_library)
 from oracle import attention as oat
 from oracle import rope as orope
 from packed_varlen_attention_gb300 import packing as pk
@@ -105,5 +106,8 @@ def test_pack_equals_samples_alone(fm, causal, block_n):
     as_bf16 = lambda x: f64(gen.f32_to_bf16_bits(x.astype(np.float32)))
     ref_o, ref_l = oat.attention_forward(as_bf16(q_rot), as_bf16(k_rot), f64(vp), cu,
                                          p.startend_row_indices, causal)
-    check_close_bf16(bf16_tensor_to_f64(out), ref_o, ATTN_MAX_ABS, ATTN_MEAN_ABS, what="pack out")
+    mag = abs_v_magnitude(lambda: (as_bf16(q_rot), as_bf16(k_rot), f64(vp)), cu,
+                          p.startend_row_indices, causal)
+    check_close_bf16(bf16_tensor_to_f64(out), ref_o, ATTN_MAX_ABS, ATTN_MEAN_ABS, what="pack out",
+                     magnitude=mag)
     check_lse(lse.cpu().numpy().astype(np.float64), ref_l, what="pack lse")

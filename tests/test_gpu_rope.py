@@ -35,22 +35,19 @@ def test_rope_full_configs(fm, cfg):
         check_close_bf16(bf16_tensor_to_f64(got), ref, ROPE_MAX_ABS, what=f"cfg{cfg} {what}")
 
 
-def test_rope_long_context_sampled(fm):
-    """131072 tokens, positions up to 65535, int64 path; sampled tokens."""
+def test_rope_long_context_full(fm):
+    """131072 tokens, positions up to 65535, int64 path; every token, in
+    chunks of 8192 tokens."""
     wl = gen.make_workload(5, seed=0)
     q, k = _run(fm, wl, force_int64=True)
     T = wl.total_tokens
-    rng = np.random.default_rng(1)
-    cu = wl.cu_seqlens.astype(np.int64)
-    toks = np.unique(np.concatenate([rng.integers(0, T, 3000), cu[:-1], cu[1:] - 1,
-                                     np.arange(65536 - 64, 65536)]))
-    toks = toks[toks < T]
-    import torch
-    idx = torch.from_numpy(toks).cuda()
-    for got, bits, what in ((q, wl.q_bits, "q"), (k, wl.k_bits, "k")):
-        ref = orope.rope_apply(gen.bf16_bits_to_f64(bits[toks]), wl.cu_seqlens, wl.theta,
-                               tokens=toks)
-        check_close_bf16(bf16_tensor_to_f64(got[idx]), ref, ROPE_MAX_ABS, what=f"cfg5 {what}")
+    for t0 in range(0, T, 8192):
+        toks = np.arange(t0, min(t0 + 8192, T))
+        for got, bits, what in ((q, wl.q_bits, "q"), (k, wl.k_bits, "k")):
+            ref = orope.rope_apply(gen.bf16_bits_to_f64(bits[toks]), wl.cu_seqlens, wl.theta,
+                                   tokens=toks)
+            check_close_bf16(bf16_tensor_to_f64(got[t0:t0 + len(toks)]), ref, ROPE_MAX_ABS,
+                             what=f"cfg5 {what} tokens {t0}+")
 
 
 def test_rope_backward_matches_oracle(fm):

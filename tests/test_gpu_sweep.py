@@ -9,7 +9,8 @@ must match the float64 oracle on sampled rows (FlashMask article, sections
 import numpy as np
 import pytest
 
-from helpers import ATTN_MAX_ABS, ATTN_MEAN_ABS, bf16_tensor_to_f64, check_close_bf16, check_lse, ensure_library
+from helpers import (ATTN_MAX_ABS, ATTN_MEAN_ABS, abs_v_magnitude, bf16_tensor_to_f64,
+                     check_close_bf16, check_lse, ensure_library)
 from oracle import attention as oat
 from oracle import mask as om
 from workloads import gen
@@ -54,6 +55,7 @@ def test_sweep_point(fm, tensors, idx):
     f64 = gen.bf16_bits_to_f64
     ro, rl = oat.attention_forward(f64(tensors[0]), f64(tensors[1]), f64(tensors[2]), cu, sri,
                                    causal, rows=rows)
+    mag = abs_v_magnitude(lambda: tuple(f64(t) for t in tensors), cu, sri, causal, rows=rows)
     check_close_bf16(bf16_tensor_to_f64(out)[rows], ro[rows], ATTN_MAX_ABS, ATTN_MEAN_ABS,
-                     what=f"{family} {param}")
+                     what=f"{family} {param}", magnitude=mag)
     check_lse(lse.cpu().numpy().astype(np.float64)[:, rows], rl[:, rows], what=f"{family} {param}")
