@@ -76,3 +76,134 @@ def test_bf16_rounding():
     assert back[1] == 1.0            # tie -> even
     assert back[2] == 1.0 + 2 ** -7  # above the tie -> up
     assert back[3] == -2.5
+
+
+# ----------------------------------------------------------------------------
+# mask recipes against brute-force predicates written from the workload text
+# (PaddleNLP FlashMask article, sections 5.1-5.2: the mask types)
+# ----------------------------------------------------------------------------
+
+from oracle import mask as om  # noqa: E402
+
+
+def _segment_masks(wl, seg):
+    """(masked, rows, cols) of segment ``seg`` from the recipe's intervals,
+    through the oracle's dense-mask builder."""
+    a, b = int(wl.cu_seqlens[seg]), int(wl.cu_seqlens[seg + 1])
+    idx = np.arange(a, b)
+    return om.dense_mask(wl.startend_row_indices[0], idx, idx, wl.causal), idx
+
+
+def _shared_question_visible(groups, i, j):
+    """Row i sees key j iff both are in one group, j <= i, and j is in the
+    group's question or i and j are in the same answer."""
+    for g0, qlen, alens in groups:
+        gend = g0 + qlen + sum(alens)
+        if not (g0 <= i < gend and g0 <= j < gend) or j > i:
+            continue
+        if j < g0 + qlen:
+            return True
+        a0 = g0 + qlen
+        for alen in alens:
+            if a0 <= i < a0 + alen and a0 <= j < a0 + alen:
+                return True
+            a0 += alen
+        return False
+    return False
+
+
+def test_shared_question_recipe_small_exhaustive():
+    groups_spec = [(3, [2, 1, 4]), (1, [1]), (4, [3, 3])]
+    groups, lens, g0 = [], [], 0
+    for qlen, alens in groups_spec:
+        groups.append((g0, qlen, alens))
+        lens.append(qlen + sum(alens))
+        g0 += lens[-1]
+    T = g0
+    sri = gen.shared_question_intervals(groups, T)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    for s in range(len(lens)):
+        idx = np.arange(cu[s], cu[s + 1])
+        masked = om.dense_mask(sri[0], idx, idx, True)
+        want = np.array([[_shared_question_visible(groups, i, j) for j in idx] for i in idx])
+        assert np.array_equal(~masked, want), s
+
+
+def test_shared_question_workload_matches_its_text():
+    """Workload 3 in full: 4 groups of one question U[512, 1536] and four
+    answers U[256, 768], total <= 16384, one segment per group; every
+    (row, key) pair of every group against the predicate."""
+    wl = gen.make_workload(3, seed=0, tensors=False)
+    assert len(wl.groups) == 4 and wl.total_tokens <= 16384
+    for s, (g0, qlen, alens) in enumerate(wl.groups):
+        assert 512 <= qlen <= 1536 and len(alens) == 4
+        assert all(256 <= x <= 768 for x in alens)
+        assert wl.cu_seqlens[s] == g0 and wl.cu_seqlens[s + 1] == g0 + qlen + sum(alens)
+        masked, idx = _segment_masks(wl, s)
+        i, j = idx[:, None], idx[None, :]
+        vis = (j <= i) & (j < g0 + qlen)
+        a0 = g0 + qlen
+        for alen in alens:
+            ina = (i >= a0) & (i < a0 + alen) & (j >= a0) & (j < a0 + alen)
+            vis |= ina & (j <= i)
+            a0 += alen
+        assert np.array_equal(~masked, vis), s
+
+
+def test_sliding_window_recipe_small_exhaustive():
+    lens = [3, 10, 7, 1]
+    W = 4
+    wl = gen.make_custom(lens, mask="window", window=W, tensors=False)
+    for s in range(len(lens)):
+        masked, idx = _segment_masks(wl, s)
+        i, j = idx[:, None], idx[None, :]
+        assert np.array_equal(~masked, (i - j >= 0) & (i - j < W)), s
+
+
+def test_long_context_window_workload_matches_its_text():
+    """Workload 5: a 65536-token document first, then documents U[512, 8192]
+    (the last one truncated), causal document mask intersected with a
+    4096-key window (row i sees key j iff same document and
+    0 <= i - j < 4096); checked on row slabs at every document start and end,
+    across the window edge and at random places."""
+    wl = gen.make_workload(5, seed=0, tensors=False)
+    cu = wl.cu_seqlens.astype(np.int64)
+    lens = np.diff(cu)
+    assert lens[0] == 65536 and np.all((lens[1:-1] >= 512) & (lens[1:-1] <= 8192))
+    assert 1 <= lens[-1] <= 8192 and cu[-1] == 131072
+    rng = np.random.default_rng(0)
+    sri = wl.startend_row_indices[0]
+    for s in range(wl.n_seqs):
+        a, b = int(cu[s]), int(cu[s + 1])
+        starts = {a, max(a, b - 96), min(b - 1, a + 4096 - 40), int(rng.integers(a, b))}
+        for r0 in starts:
+            rows = np.arange(r0, min(r0 + 96, b))
+            cols = np.arange(a, b)
+            masked = om.dense_mask(sri, rows, cols, True)
+            d = rows[:, None] - cols[None, :]
+            assert np.array_equal(~masked, (d >= 0) & (d < 4096)), (s, r0)
+
+
+def test_headline_causal_document_matches_its_text():
+    wl = gen.make_workload(2, seed=0, tensors=False)
+    for s in range(wl.n_seqs):
+        masked, idx = _segment_masks(wl, s)
+        assert np.array_equal(~masked, idx[:, None] >= idx[None, :]), s
+
+
+def test_bidirectional_prefix_lm_workload_matches_its_text():
+    """Workload 4 (non-causal): even documents fully bidirectional; odd
+    documents prefix-LM, the first floor(len / 4) tokens visible to the whole
+    document and later keys only to rows at or after them."""
+    for alt in (False, True):
+        wl = gen.make_workload(4, seed=0, tensors=False, alt_mask=alt)
+        assert not wl.causal
+        for s in range(wl.n_seqs):
+            masked, idx = _segment_masks(wl, s)
+            a, b = int(wl.cu_seqlens[s]), int(wl.cu_seqlens[s + 1])
+            i, j = idx[:, None], idx[None, :]
+            if s % 2 == 0:
+                want = np.ones(masked.shape, dtype=bool)
+            else:
+                want = (j < a + (b - a) // 4) | (j <= i)
+            assert np.array_equal(~masked, want), (alt, s)

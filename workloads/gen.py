@@ -80,6 +80,8 @@ class Workload:
     cu_seqlens: np.ndarray                     # int32 [n_seqs + 1]
     startend_row_indices: Optional[np.ndarray]  # int32 [Hm][4][T] or None
     doc_kinds: List[str] = field(default_factory=list)
+    # shared-question workloads: (group start, question length, [answer lengths])
+    groups: List[tuple] = field(default_factory=list)
     q_bits: Optional[np.ndarray] = None        # uint16 [T, Hq, D]
     k_bits: Optional[np.ndarray] = None        # uint16 [T, Hkv, D]
     v_bits: Optional[np.ndarray] = None        # uint16 [T, Hkv, D]
@@ -355,7 +357,8 @@ def make_workload(cfg: int, seed: int = 0, tensors: bool = True,
             g0 += ql + sum(al)
         cu = _cu_from_lens(glens)
         wl = Workload(CONFIG_NAMES[3], T, 32, 32, 128, 1.0e4, True, 128, 128, False,
-                      cu, shared_question_intervals(groups, T), ["shared_question"] * 4)
+                      cu, shared_question_intervals(groups, T), ["shared_question"] * 4,
+                      groups=groups)
     elif cfg == 4:
         T = 16384
         lens = _fill_until_full(rng, T, lambda: rng.integers(256, 4096, endpoint=True))
