@@ -241,7 +241,9 @@ FM_API fm_status fm_attn_fwd_varlen(const void* q, const void* k, const void* v,
  * make that first call before any stream capture.  All calls on a device
  * share the array and each call clears what must start at zero; calls that
  * overlap on the GPU race on it, so order them on one stream.  Nothing is
- * allocated or freed.
+ * allocated or freed.  The device error word and the timeout record of the
+ * last call on the current device are read with fm_get_device_error /
+ * fm_get_device_timeout_info given workspace == NULL.
  */
 FM_API fm_status fm_attn_fwd_varlen_noalloc(const void* q, const void* k, const void* v,
                                             int64_t total_tokens, int n_heads_q, int n_heads_kv,
@@ -355,6 +357,8 @@ FM_API fm_status fm_attn_fwd_num_work_items(const void* workspace, int64_t* host
  * fm_get_device_error -- synchronises `stream` and copies the device error
  * word of the last fm_attn_fwd_varlen or fm_attn_bwd_varlen that used
  * `workspace` into *host_err (a bit set of FM_DEVERR_*; 0 when clean).
+ * workspace == NULL reads the word of the last fm_attn_fwd_varlen_noalloc
+ * call on the current device (its array inside the library).
  */
 FM_API fm_status fm_get_device_error(const void* workspace, int32_t* host_err, void* stream);
 
@@ -363,7 +367,8 @@ FM_API fm_status fm_get_device_error(const void* workspace, int32_t* host_err, v
  * describing the first pipeline wait that ran out in the last call that used
  * `workspace`: {1 if one did (else 0), barrier index, phase parity,
  * block << 8 | warp}.  Barrier indices are internal to each kernel; this is
- * a diagnostic for bug reports, not an interface to act on.
+ * a diagnostic for bug reports, not an interface to act on.  workspace ==
+ * NULL: the last fm_attn_fwd_varlen_noalloc call on the current device.
  */
 FM_API fm_status fm_get_device_timeout_info(const void* workspace, int32_t* host_info, void* stream);
 

@@ -411,15 +411,19 @@ def attn_fwd_num_work_items(workspace: torch.Tensor, stream=None) -> int:
     return int(n.value)
 
 
-def get_device_error(workspace: torch.Tensor, stream=None) -> int:
+def get_device_error(workspace: Optional[torch.Tensor], stream=None) -> int:
+    """Device error word (FM_DEVERR_* bits) of the last call that used
+    ``workspace``; ``None``: the last ``attn_fwd_varlen_noalloc`` call on the
+    current device."""
     e = ctypes.c_int32(0)
     _check("fm_get_device_error",
            _lib().fm_get_device_error(_ptr(workspace), ctypes.byref(e), _stream(stream)))
     return int(e.value)
 
 
-def get_device_timeout_info(workspace: torch.Tensor, stream=None):
-    """(expired, barrier, parity, block, warp) of the first wait that ran out."""
+def get_device_timeout_info(workspace: Optional[torch.Tensor], stream=None):
+    """(expired, barrier, parity, block, warp) of the first wait that ran out
+    (``workspace=None``: the last ``attn_fwd_varlen_noalloc`` call)."""
     info = (ctypes.c_int32 * 4)()
     _check("fm_get_device_timeout_info", _lib().fm_get_device_timeout_info(
         _ptr(workspace), info, _stream(stream)))

@@ -15,7 +15,9 @@
 // contents; each call's planner first initialises the part that must start
 // at zero (work counter, error word), exactly as with a caller workspace.
 // Calls that overlap on the GPU (different streams without ordering) race
-// on the array and give wrong results: order them on one stream.
+// on the array and give wrong results: order them on one stream.  The array
+// starts with the same header as a caller workspace, so fm_get_device_error
+// and fm_get_device_timeout_info read its error word when given NULL.
 #include <mutex>
 
 #include "fm_internal.h"
@@ -34,10 +36,10 @@ static_assert(kScratchBytes % 256 == 0, "scratch size is a multiple of 256 bytes
 
 static __device__ __align__(256) uint8_t g_attn_scratch[kScratchBytes];
 
-namespace {
+namespace fm {
 
 // Device address of g_attn_scratch, resolved once per device.
-void* scratch_address(fm_status* st) {
+void* noalloc_scratch_address(fm_status* st) {
   static void* addr[kMaxDevices] = {};
   static std::mutex mu;
   int dev = 0;
@@ -62,7 +64,7 @@ void* scratch_address(fm_status* st) {
   return addr[dev];
 }
 
-}  // namespace
+}  // namespace fm
 
 extern "C" fm_status fm_attn_fwd_varlen_noalloc(
     const void* q, const void* k, const void* v, int64_t total_tokens, int n_heads_q,
@@ -76,7 +78,7 @@ extern "C" fm_status fm_attn_fwd_varlen_noalloc(
   if (fm::attn_workspace_bytes(total_tokens, n_seqs, block_m) > kScratchBytes)
     return FM_ERR_WORKSPACE;
   fm_status st = FM_OK;
-  void* scratch = scratch_address(&st);
+  void* scratch = fm::noalloc_scratch_address(&st);
   if (st != FM_OK) return st;
   return fm_attn_fwd_varlen(q, k, v, total_tokens, n_heads_q, n_heads_kv, head_dim, cu_seqlens,
                             n_seqs, startend_row_indices, n_mask_heads, block_minmax, causal,

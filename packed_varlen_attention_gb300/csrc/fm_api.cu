@@ -445,7 +445,13 @@ fm_status fm_attn_fwd_num_work_items(const void* workspace, int64_t* host_items,
 }
 
 fm_status fm_get_device_error(const void* workspace, int32_t* host_err, void* stream) {
-  if (workspace == nullptr || host_err == nullptr) return FM_ERR_INVALID_ARG;
+  if (host_err == nullptr) return FM_ERR_INVALID_ARG;
+  if (workspace == nullptr) {
+    // the allocation-free entry point's array on the current device
+    fm_status st = FM_OK;
+    workspace = fm::noalloc_scratch_address(&st);
+    if (st != FM_OK) return st;
+  }
   const auto* hdr = static_cast<const fm::AttnWorkspaceHeader*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(host_err, &hdr->error_word, sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
@@ -456,7 +462,12 @@ fm_status fm_get_device_error(const void* workspace, int32_t* host_err, void* st
 }
 
 fm_status fm_get_device_timeout_info(const void* workspace, int32_t* host_info, void* stream) {
-  if (workspace == nullptr || host_info == nullptr) return FM_ERR_INVALID_ARG;
+  if (host_info == nullptr) return FM_ERR_INVALID_ARG;
+  if (workspace == nullptr) {
+    fm_status st = FM_OK;
+    workspace = fm::noalloc_scratch_address(&st);
+    if (st != FM_OK) return st;
+  }
   const auto* hdr = static_cast<const fm::AttnWorkspaceHeader*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(host_info, hdr->diag, sizeof(hdr->diag), cudaMemcpyDeviceToHost, s) !=

@@ -103,6 +103,10 @@ struct AttnParams {
 
 size_t attn_workspace_bytes(int64_t T, int n_seqs, int block_m);
 
+// Device address of the allocation-free entry point's scheduler array on the
+// current device (resolved once per device); nullptr with *st set on failure.
+void* noalloc_scratch_address(fm_status* st);
+
 // rope == nullptr: q is already rotated; otherwise every Q tile is rotated
 // in shared memory after its load (positions restart at each sample start).
 cudaError_t launch_attn_fwd(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
