@@ -245,12 +245,19 @@ __global__ void __launch_bounds__(256) plan_cost_kernel(const AttnParams p) {
   const int r1 = min(r0 + p.block_m, b);
   const int r2 = min(r0 + BM2, b);
   const int kt_end = kv_tiles_to_scan<BN>(p, a, b, r2);
+  // With one mask per q head the pair's items differ in cost; the order
+  // uses the costliest head's count (all heads of a pair run side by side).
+  const int n_mh = p.hm > 1 ? p.hm : 1;
   int cost = 0;
-  for (int base = 0; base < kt_end; base += 32) {
-    int c0, c1;
-    tile_classes<BN>(p, 0, s, a, b, r0, r1, r2, base + lane, kt_end, c0, c1);
-    cost += __popc(__ballot_sync(0xffffffffu, c0 != kClsF));
-    cost += __popc(__ballot_sync(0xffffffffu, c1 != kClsF));
+  for (int mh = 0; mh < n_mh; ++mh) {
+    int c = 0;
+    for (int base = 0; base < kt_end; base += 32) {
+      int c0, c1;
+      tile_classes<BN>(p, mh, s, a, b, r0, r1, r2, base + lane, kt_end, c0, c1);
+      c += __popc(__ballot_sync(0xffffffffu, c0 != kClsF));
+      c += __popc(__ballot_sync(0xffffffffu, c1 != kClsF));
+    }
+    cost = max(cost, c);
   }
   if (lane == 0) {
     p.cost[u] = cost * 2 + (r2 > r1 ? 1 : 0);
