@@ -203,9 +203,13 @@ class ClockSampler:
                 "power_w_max": float(max(power))}
 
 
-def measured_traffic():
-    """DRAM bytes per attention launch from the committed ncu capture, or None
-    when the kernel source changed since that capture."""
+def stored_traffic():
+    """DRAM bytes per attention launch, per workload, from the committed ncu
+    captures (profiles/attn_fwd_dram_traffic.json): {workload: {read, write,
+    command}}, or {} when the kernel sources changed since the capture (the
+    file keeps a hash of them).  The counters come from one ncu capture per
+    workload, not from this run, and ncu closes the kernel before the output
+    lines still held in L2 are written back, so `write` undercounts."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "attn_fwd_dram_traffic.json")
     try:
@@ -216,10 +220,35 @@ def measured_traffic():
             with open(os.path.join(ROOT, src), "rb") as g:
                 h.update(g.read())
         if h.hexdigest() != d["source_sha256"]:
-            return None
-        return int(d["dram_bytes_read"]) + int(d["dram_bytes_write"])
+            return {}
+        return {w: {"read": int(e["dram_bytes_read"]), "write": int(e["dram_bytes_write"]),
+                    "command": e["command"]} for w, e in d["workloads"].items()}
     except (OSError, ValueError, KeyError):
+        return {}
+
+
+def attn_algorithmic_bytes(wl):
+    """Bytes the attention call must move at least: q, k, v read once; out and
+    lse written once."""
+    T, hq, hkv, D = wl.total_tokens, wl.n_heads_q, wl.n_heads_kv, wl.head_dim
+    read = T * hq * D * 2 + 2 * T * hkv * D * 2
+    write = T * hq * D * 2 + hq * T * 4
+    return read, write
+
+
+def traffic_entry(wl, traffic):
+    """DRAM traffic of the stored capture for this workload against the
+    algorithmic bytes (reads above them are re-reads of K/V tiles that fell
+    out of L2)."""
+    e = traffic.get(wl.name)
+    if e is None:
         return None
+    a_read, a_write = attn_algorithmic_bytes(wl)
+    return {"dram_read_bytes": e["read"], "dram_write_bytes": e["write"],
+            "algorithmic_read_bytes": a_read, "algorithmic_write_bytes": a_write,
+            "read_over_algorithmic": e["read"] / a_read,
+            "source": "stored ncu capture (profiles/attn_fwd_dram_traffic.json); writes still "
+                      "in L2 when the kernel ends are not counted"}
 
 
 def replica_throughput(torch, world, flop_per_step, steps, ms_totals, device="cpu"):
@@ -511,6 +540,7 @@ def run_ours(args):
     import packed_varlen_attention_gb300 as fm
     peaks, peak_src = load_peaks()
     flush = L2Flush(torch, device)
+    traffic = stored_traffic()
 
     cfgs = [HEADLINE_CFG] if args.configs == "headline" else [1, 2, 3, 4, 5]
     per_config = {}
@@ -537,6 +567,7 @@ def run_ours(args):
             "block_counts_fpu": counts.cpu().tolist(),
             "tokens": wl.total_tokens,
             **tile_accounting(wl, counts.cpu().tolist(), t["attn_ms"]),
+            "dram_traffic": traffic_entry(wl, traffic),
         }
         per_config[gen.CONFIG_NAMES[cfg]]["fused_rope"] = fused_entry(
             fl, time_fused(fm, torch, b, max(5, min(args.steps, 20)), 3, flush), t["step_ms"])
@@ -654,6 +685,7 @@ def run_ours(args):
         "step_ms": float(np.mean(step_ms)), "effective_tflop_per_step": fl / 1e12,
         "block_counts_fpu": counts.cpu().tolist(), "tokens": wl.total_tokens,
         **tile_accounting(wl, counts.cpu().tolist(), attn_ms),
+        "dram_traffic": traffic_entry(wl, traffic),
         "backward": backward_entry(fl, bwd_ms, peaks),
         "fused_rope": fused_entry(fl, fused_ms, float(np.mean(step_ms))),
         "cuda_graph_step": {"ms": graph_ms, "effective_tflops": fl / (graph_ms * 1e-3) / 1e12,
@@ -689,8 +721,13 @@ def run_ours(args):
             "unit": "TFLOP/s",
             "frac": attn_tflops / peaks["bf16_tflops"],
             "peak_source": f"{peak_src} bf16 burst",
-            "traffic": measured_traffic(),
-            "traffic_unit": "bytes per launch (ncu dram read + write, headline workload)",
+            "traffic": (lambda e: None if e is None else e["read"] + e["write"])(
+                traffic.get(gen.CONFIG_NAMES[HEADLINE_CFG])),
+            "traffic_unit": "bytes per launch: dram__bytes_read.sum + dram__bytes_write.sum of "
+                            "the stored ncu capture of this kernel on this workload (null once "
+                            "the kernel sources differ from the captured ones); ncu closes the "
+                            "kernel before the output lines still in L2 are written back, so "
+                            "the write part undercounts",
         },
         "backward": dict(backward_entry(fl, bwd_ms, peaks), **{
             "call": "attn_bwd_varlen (prep + dK/dV kernel + dQ kernel), same batch, dout seeded",
@@ -891,6 +928,19 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one replica per GPU: relaunch this command under torchrun
+        import socket
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+               f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+               "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+        sys.exit(subprocess.call(cmd))
+    if "WORLD_SIZE" in os.environ and int(os.environ["WORLD_SIZE"]) != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={os.environ['WORLD_SIZE']}; "
+              f"running {os.environ['WORLD_SIZE']} replicas", file=sys.stderr)
     if args.sweep == "sparsity":
         if args.steps == 50:
             args.steps = 10
