@@ -62,7 +62,6 @@ namespace {
 // warps 0..3: K producer, MMA issuer(s), V producer; warps 4.. : one softmax
 // warpgroup per Q tile of an item (warp w reads TMEM lanes 32*(w%4)..+31).
 constexpr int kFirstSoftmaxWarp = 4;
-constexpr int kStages = 2;
 constexpr int kTileM = 128;  // MMA M: TMEM lanes = tile rows
 constexpr int kMetaSlots = 4;
 // Interval-masked tiles whose columns form at most this many runs of equal
@@ -70,11 +69,27 @@ constexpr int kMetaSlots = 4;
 constexpr int kMaxRuns = 8;
 constexpr int kPrefetchAhead = 3;  // K/V tiles pulled into L2 ahead of their loads
 
+// Shared-memory rings.  K and V tiles share one ring of kKVSlots slots,
+// loaded in the order K(0), V(0), K(1), V(1), ... of the CTA's KV tiles
+// (load p into slot p mod kKVSlots): with three slots, K(t+2) takes the slot
+// V(t) leaves once the PV MMAs of tile t are done, one KV step before S(t+2)
+// needs it.  Q tiles have their own ring of kQSlots tile buffers, filled in
+// work order (tile 0, then tile 1 of each item), so the next item's first Q
+// tile lands while the current item still runs and its second one as soon
+// as the current item's tile 0 has had its last S MMA.  Three K/V slots and
+// three Q tiles of 32 KB take the shared memory that two K stages, two V
+// stages and one pair of Q tiles took before.
+template <int BN>
+constexpr int kKVSlots = 4;
+template <int BN>
+constexpr int kQSlots = (BN == 128) ? 2 : 4;
+constexpr int kMaxKVSlots = 4;
+constexpr int kMaxQSlots = 4;
+
 // With 64-column key tiles TMEM holds two S buffers per Q tile (S_i of KV
 // tile t+2 is computed into the buffer PV_i of tile t has just read, while
-// the softmax works on tile t+1) and shared memory two Q buffers (the next
-// item's Q tiles land while the current item runs).  128-column key tiles
-// fill TMEM with one S per Q tile.
+// the softmax works on tile t+1).  128-column key tiles fill TMEM with one S
+// per Q tile.
 //
 // QT = Q tiles per work item (one softmax warpgroup each).  QT = 2 shares
 // every K/V tile between two Q tiles; TMEM then holds two S buffers per Q
@@ -82,7 +97,7 @@ constexpr int kPrefetchAhead = 3;  // K/V tiles pulled into L2 ahead of their lo
 // 128-column S buffers, so the single softmax warpgroup never waits for its
 // own tile's MMAs.
 template <int BN, int QT>
-constexpr int kBufs = (QT == 1 || BN == 64) ? 2 : 1;
+constexpr int kSBufs = (QT == 1 || BN == 64) ? 2 : 1;
 
 // MMA issuing warps: each Q tile has its own issuer (warps 1 and 3), so one
 // tile's barrier waits never hold up the other tile's MMAs.
@@ -113,28 +128,28 @@ struct TileMeta {
   int h, kvh;      // q head, key/value head
   int n_runs;      // partial tiles: runs of equal intervals in the run table, 0 = per column
   int a;           // first row of the sample (RoPE positions count from it)
-  int pad[5];
+  int qseq;        // Q ring position of the item's tile 0 (tile 1: qseq + 1)
+  int pad[4];
 };
 static_assert(sizeof(TileMeta) == 64, "TileMeta is 64 bytes");
 
 enum Bar : int {
-  kKFull = 0,                     // [kStages]  K tile landed (TMA tx)
-  kKEmpty = kKFull + kStages,      // [kStages]  S MMAs done reading K
-  kVFull = kKEmpty + kStages,      // [kStages]  V tile landed
-  kVEmpty = kVFull + kStages,      // [kStages]  PV MMAs done reading V
-  kMFull = kVEmpty + kStages,      // [kMetaSlots] tile metadata written
-  kMEmpty = kMFull + kMetaSlots,   // [kMetaSlots] metadata consumed
-  kQFull = kMEmpty + kMetaSlots,   // [2 buffers] both Q tiles of an item landed
-  kQEmpty = kQFull + 2,            // [2 buffers] last S MMA of the item done
-  kSFull = kQEmpty + 2,            // [2 tiles][2 buffers] S_i ready
+  kKVFull = 0,                        // [kMaxKVSlots] K or V tile landed (TMA tx)
+  kKVEmpty = kKVFull + kMaxKVSlots,   // [kMaxKVSlots] both issuers' MMAs done reading it
+  kMFull = kKVEmpty + kMaxKVSlots,    // [kMetaSlots] tile metadata written
+  kMEmpty = kMFull + kMetaSlots,      // [kMetaSlots] metadata consumed
+  kQFull = kMEmpty + kMetaSlots,      // [kMaxQSlots] Q tile landed
+  kQEmpty = kQFull + kMaxQSlots,      // [kMaxQSlots] last S MMA on it done (fused RoPE: and
+                                      //   its 128 rows rotated and copied out)
+  kSFull = kQEmpty + kMaxQSlots,      // [2 tiles][2 buffers] S_i ready
   kPFull = kSFull + 4,             // [2 tiles][2 buffers] P_i written (128 arrivals)
   kOFull = kPFull + 4,             // [2] last PV_i of the item done (one S buffer)
   kPVDone = kOFull + 2,            // [2 tiles][2 buffers] PV_i done (two S buffers)
   kOEmpty = kPVDone + 4,           // [2] O_i read by the epilogue (128 arrivals)
   kDrain = kOEmpty + 2,            // [2] an issuer's MMAs are all done
   kTurn = kDrain + 2,              // [2] issuer i may issue its next block
-  kQRot = kTurn + 2,               // [2 tiles][2 buffers] Q_i rotated in place (128 arrivals)
-  kNumBars = kQRot + 4
+  kQRot = kTurn + 2,                  // [kMaxQSlots] Q tile rotated in place (128 arrivals)
+  kNumBars = kQRot + kMaxQSlots
 };
 
 // arrivals on kMEmpty: the V producer lane, the MMA issuers and the softmax
@@ -145,12 +160,10 @@ constexpr int kMEmptyCount = 1 + kIssuers<QT> + 4 * QT;
 template <int D, int BN, int QT>
 struct Layout {
   static constexpr int kQBytes = kTileM * D * 2;  // one Q tile
-  static constexpr int kKBytes = BN * D * 2;
-  static constexpr int kVBytes = BN * D * 2;
-  static constexpr int kQ = 0;  // kBufs buffers of QT Q tiles
-  static constexpr int kK = kQ + kBufs<BN, QT> * QT * kQBytes;
-  static constexpr int kV = kK + kStages * kKBytes;
-  static constexpr int kCols = kV + kStages * kVBytes;  // int32 [kMetaSlots][4][BN]
+  static constexpr int kKVBytes = BN * D * 2;     // one K or V tile
+  static constexpr int kQ = 0;                    // kQSlots Q tile buffers
+  static constexpr int kKV = kQ + kQSlots<BN> * kQBytes;  // kKVSlots K/V slots
+  static constexpr int kCols = kKV + kKVSlots<BN> * kKVBytes;  // int32 [kMetaSlots][4][BN]
   static constexpr int kMeta = kCols + kMetaSlots * 4 * BN * 4;
   // int32 [kMetaSlots][kMaxRuns][8]: start column, LTS, LTE, UTS, UTE of each run
   static constexpr int kRuns = kMeta + kMetaSlots * static_cast<int>(sizeof(TileMeta));
@@ -163,12 +176,14 @@ struct Layout {
   static constexpr int kEnd = kAbort + 4;
   static constexpr int kBytes = kEnd + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  // TMEM columns: S_i of buffer b at (i*kBufs + b)*BN (P_i packed into its
+  // TMEM columns: S_i of buffer b at (i*kSBufs + b)*BN (P_i packed into its
   // first BN/2 columns), O_i at 256 + i*128.
   __host__ __device__ static constexpr uint32_t s_col(int i, uint32_t b) {
-    return static_cast<uint32_t>((i * kBufs<BN, QT> + static_cast<int>(b)) * BN);
+    return static_cast<uint32_t>((i * kSBufs<BN, QT> + static_cast<int>(b)) * BN);
   }
-  static_assert(QT * kBufs<BN, QT> * BN <= 256, "S buffers fit below the O columns");
+  static_assert(QT * kSBufs<BN, QT> * BN <= 256, "S buffers fit below the O columns");
+  static_assert(kKVSlots<BN> <= kMaxKVSlots && kQSlots<BN> <= kMaxQSlots, "ring sizes");
+  static_assert(kQSlots<BN> >= QT, "an item's Q tiles fit in the ring");
   static_assert(BN <= 128 && D <= 128, "TMEM budget");
   static_assert(kBytes <= 232448, "shared memory budget");
 };
@@ -417,19 +432,22 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
   const int BM = p.block_m;
   const Sync sy{bars, abort_flag, p.timeout_ns, &p.ws->error_word, lane};
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&bars[kKFull + i], 1);
-      mbar_init(&bars[kKEmpty + i], kIssuers<QT>);
-      mbar_init(&bars[kVFull + i], 1);
-      mbar_init(&bars[kVEmpty + i], kIssuers<QT>);
+    for (int i = 0; i < kKVSlots<BN>; ++i) {
+      mbar_init(&bars[kKVFull + i], 1);
+      mbar_init(&bars[kKVEmpty + i], kIssuers<QT>);
+    }
+    for (int i = 0; i < kQSlots<BN>; ++i) {
+      mbar_init(&bars[kQFull + i], 1);
+      // the tile's issuer commits after its last S MMA; with the fused RoPE
+      // the 128 threads that rotate (and copy out) the tile arrive as well
+      mbar_init(&bars[kQEmpty + i], ROPE ? 1 + 128 : 1);
+      mbar_init(&bars[kQRot + i], 128);
     }
     for (int i = 0; i < kMetaSlots; ++i) {
       mbar_init(&bars[kMFull + i], 1);
       mbar_init(&bars[kMEmpty + i], kMEmptyCount<QT>);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[kQFull + i], 1);
-      mbar_init(&bars[kQEmpty + i], kIssuers<QT>);
       mbar_init(&bars[kOFull + i], 1);
       mbar_init(&bars[kOEmpty + i], 128);
     }
@@ -437,7 +455,6 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       mbar_init(&bars[kPVDone + i], 1);
       mbar_init(&bars[kSFull + i], 1);
       mbar_init(&bars[kPFull + i], 128);
-      mbar_init(&bars[kQRot + i], 128);
     }
     mbar_init(&bars[kDrain], 1);
     mbar_init(&bars[kDrain + 1], 1);
@@ -463,16 +480,20 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
     // --------------------------------------------------- K producer + metadata
     const int n_items = p.ws->n_items;
     const int group = p.hq / p.hkv;
-    uint32_t kst = 0, kround = 0;    // K ring
+    constexpr uint32_t NKV = kKVSlots<BN>, NQ = kQSlots<BN>;
+    uint32_t kv_t = 0;               // KV tiles loaded (K(t) is ring load 2t)
     uint32_t mslot = 0, mround = 0;  // metadata ring
-    uint32_t q_round = 0;
-    uint32_t k_armed[kStages] = {0xffffffffu, 0xffffffffu};
-    uint32_t q_armed[2] = {0xffffffffu, 0xffffffffu};
+    uint32_t q_seq = 0;              // Q tiles loaded (Q ring position)
+    uint32_t k_armed[kMaxKVSlots], q_armed[kMaxQSlots];  // ring position last armed, per slot
+#pragma unroll
+    for (int i = 0; i < kMaxKVSlots; ++i) k_armed[i] = 0xffffffffu;
+#pragma unroll
+    for (int i = 0; i < kMaxQSlots; ++i) q_armed[i] = 0xffffffffu;
     long long cnt_p = 0, cnt_u = 0, cnt_f = 0;
     bool ok = true;
 
     auto push_meta = [&](int flags, int cls0, int cls1, int c0, int c1, int r0, int r_end, int h,
-                         int kvh, bool copy_cols, int mh, int a) -> bool {
+                         int kvh, bool copy_cols, int mh, int a, uint32_t qseq) -> bool {
       if (!sy.warp(kMEmpty + mslot, (mround & 1) ^ 1)) return false;
       int n_runs = 0;
       if (copy_cols) {
@@ -534,6 +555,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         m.h = h;
         m.kvh = kvh;
         m.a = a;
+        m.qseq = static_cast<int>(qseq);
       }
       __threadfence_block();
       __syncwarp();
@@ -545,12 +567,28 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       return true;
     };
 
+    // Q ring position u -> buffer u % NQ, once the MMAs (and, with the fused
+    // RoPE, the rotation) of the tile held there before are done
+    auto load_q = [&](uint32_t u, int h, int row0) -> bool {
+      const uint32_t b = u % NQ;
+      if (!sy.warp(kQEmpty + b, ((u / NQ) & 1u) ^ 1u)) return false;
+      if (lane == 0) {
+        uint8_t* qdst = smem + L::kQ + b * L::kQBytes;
+        mbar_arrive_expect_tx(&bars[kQFull + b], L::kQBytes);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(qdst + c * (kTileM * 128), &tq, &bars[kQFull + b], h * D + c * 64, row0);
+      }
+      q_armed[b] = u;
+      return true;
+    };
+
     while (ok) {
       int item = 0;
       if (lane == 0) item = static_cast<int>(atomicAdd(&p.ws->work_counter, 1u));
       item = __shfl_sync(0xffffffffu, item, 0);
       if (item >= n_items) {
-        ok = push_meta(kStop, kClsF, kClsF, 0, 0, 0, 0, 0, 0, false, 0, 0);
+        ok = push_meta(kStop, kClsF, kClsF, 0, 0, 0, 0, 0, 0, false, 0, 0, 0u);
         break;
       }
       const int2 pi = p.order[item / p.hq];
@@ -663,50 +701,40 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
           const int flags = (pushed == 0 ? kFirst : 0) | (pushed == n_live - 1 ? kLast : 0) |
                             (has_q1 ? kHasQ1 : 0);
           const bool copy = (cls0 == kClsP || cls1 == kClsP) && p.sri != nullptr;
-          if (!push_meta(flags, cls0, cls1, c0, c1, r0, r2, h, kvh, copy, mh, a)) {
+          if (!push_meta(flags, cls0, cls1, c0, c1, r0, r2, h, kvh, copy, mh, a, q_seq)) {
             ok = false;
             break;
           }
-          if (pushed == 0) {
-            // Q tiles of this item into Q buffer q_round % kBufs, once the S
-            // MMAs of the item that used that buffer last are done
-            const uint32_t qb = q_round % kBufs<BN, QT>;
-            if (!sy.warp(kQEmpty + qb, ((q_round / kBufs<BN, QT>) & 1) ^ 1)) {
+          // the item's Q tile 0 first (its buffer was freed long before), then
+          // K of the first tile, then Q tile 1, whose buffer frees when the
+          // previous item's tile 0 has had its last S MMA
+          if (pushed == 0 && !load_q(q_seq, h, r0)) {
+            ok = false;
+            break;
+          }
+          {
+            const uint32_t pos = 2u * kv_t;  // K(t): even ring loads
+            const uint32_t slot = pos % NKV;
+            if (!sy.warp(kKVEmpty + slot, ((pos / NKV) & 1u) ^ 1u)) {
               ok = false;
               break;
             }
             if (lane == 0) {
-              uint8_t* qdst = smem + L::kQ + qb * QT * L::kQBytes;
-              mbar_arrive_expect_tx(&bars[kQFull + qb], (has_q1 ? 2 : 1) * L::kQBytes);
+              mbar_arrive_expect_tx(&bars[kKVFull + slot], L::kKVBytes);
 #pragma unroll
               for (int c = 0; c < D / 64; ++c)
-                tma_load_2d(qdst + c * (kTileM * 128), &tq, &bars[kQFull + qb],
-                            h * D + c * 64, r0);
-              if (has_q1) {
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                  tma_load_2d(qdst + L::kQBytes + c * (kTileM * 128), &tq,
-                              &bars[kQFull + qb], h * D + c * 64, r0 + BM);
-              }
+                tma_load_2d(smem + L::kKV + slot * L::kKVBytes + c * (BN * 128), &tk,
+                            &bars[kKVFull + slot], kvh * D + c * 64, c0);
             }
-            q_armed[qb] = q_round;
-            ++q_round;
+            k_armed[slot] = pos;
+            ++kv_t;
           }
-          if (!sy.warp(kKEmpty + kst, (kround & 1) ^ 1)) {
-            ok = false;
-            break;
-          }
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&bars[kKFull + kst], L::kKBytes);
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-              tma_load_2d(smem + L::kK + kst * L::kKBytes + c * (BN * 128), &tk,
-                          &bars[kKFull + kst], kvh * D + c * 64, c0);
-          }
-          k_armed[kst] = kround;
-          if (++kst == kStages) {
-            kst = 0;
-            ++kround;
+          if (pushed == 0) {
+            if (has_q1 && !load_q(q_seq + 1u, h, r0 + BM)) {
+              ok = false;
+              break;
+            }
+            q_seq += has_q1 ? 2u : 1u;
           }
           ++pushed;
         }
@@ -714,13 +742,12 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
     }
     if (!ok) {
       // let every TMA load this warp issued land before the CTA exits
-      for (int st = 0; st < kStages; ++st)
+      for (uint32_t st = 0; st < NKV; ++st)
         if (k_armed[st] != 0xffffffffu)
-          mbar_wait_bounded(&bars[kKFull + st], k_armed[st] & 1, 100000000ull, nullptr);
-      for (int qb = 0; qb < 2; ++qb)
+          mbar_wait_bounded(&bars[kKVFull + st], (k_armed[st] / NKV) & 1u, 100000000ull, nullptr);
+      for (uint32_t qb = 0; qb < NQ; ++qb)
         if (q_armed[qb] != 0xffffffffu)
-          mbar_wait_bounded(&bars[kQFull + qb], (q_armed[qb] / kBufs<BN, QT>) & 1, 100000000ull,
-                            nullptr);
+          mbar_wait_bounded(&bars[kQFull + qb], (q_armed[qb] / NQ) & 1u, 100000000ull, nullptr);
     }
     if (lane == 0 && p.class_counts != nullptr) {
       atomicAdd(reinterpret_cast<unsigned long long*>(p.class_counts + 0),
@@ -735,8 +762,11 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
   } else if (warp == 2) {
     // --------------------------------------------------------------- V producer
     if (lane == 0) {
-      uint32_t vst = 0, vround = 0, mslot = 0, mround = 0;
-      uint32_t v_armed[kStages] = {0xffffffffu, 0xffffffffu};
+      constexpr uint32_t NKV = kKVSlots<BN>;
+      uint32_t v_t = 0, mslot = 0, mround = 0;  // V(t) is ring load 2t + 1
+      uint32_t v_armed[kMaxKVSlots];
+#pragma unroll
+      for (int i = 0; i < kMaxKVSlots; ++i) v_armed[i] = 0xffffffffu;
       bool ok = true;
       for (;;) {
         if (!sy.lone(kMFull + mslot, mround & 1)) { ok = false; break; }
@@ -749,22 +779,22 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
           ++mround;
         }
         if (flags & kStop) break;
-        if (!sy.lone(kVEmpty + vst, (vround & 1) ^ 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(&bars[kVFull + vst], L::kVBytes);
+        const uint32_t pos = 2u * v_t + 1u;
+        const uint32_t slot = pos % NKV;
+        if (!sy.lone(kKVEmpty + slot, ((pos / NKV) & 1u) ^ 1u)) { ok = false; break; }
+        mbar_arrive_expect_tx(&bars[kKVFull + slot], L::kKVBytes);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_2d(smem + L::kV + vst * L::kVBytes + c * (BN * 128), &tv,
-                      &bars[kVFull + vst], kvh * D + c * 64, c0);
-        v_armed[vst] = vround;
-        if (++vst == kStages) {
-          vst = 0;
-          ++vround;
-        }
+          tma_load_2d(smem + L::kKV + slot * L::kKVBytes + c * (BN * 128), &tv,
+                      &bars[kKVFull + slot], kvh * D + c * 64, c0);
+        v_armed[slot] = pos;
+        ++v_t;
       }
       if (!ok) {
-        for (int st = 0; st < kStages; ++st)
+        for (uint32_t st = 0; st < NKV; ++st)
           if (v_armed[st] != 0xffffffffu)
-            mbar_wait_bounded(&bars[kVFull + st], v_armed[st] & 1, 100000000ull, nullptr);
+            mbar_wait_bounded(&bars[kKVFull + st], (v_armed[st] / NKV) & 1u, 100000000ull,
+                              nullptr);
       }
     }
     attn_teardown<D, BN, QT>(tmem_slot, warp);
@@ -779,20 +809,25 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       const int me = warp == 1 ? 0 : 1;
       constexpr uint32_t kIdescS = idesc_bf16_f32(kTileM, BN, false);
       constexpr uint32_t kIdescO = idesc_bf16_f32(kTileM, D, true);
+      constexpr uint32_t NKV = kKVSlots<BN>, NQ = kQSlots<BN>;
       const uint32_t q_addr = smem_u32(smem + L::kQ);
-      const uint32_t k_addr = smem_u32(smem + L::kK);
-      const uint32_t v_addr = smem_u32(smem + L::kV);
+      const uint32_t kv_addr = smem_u32(smem + L::kKV);
       uint32_t mslot = 0, mround = 0;  // metadata ring (released by the other readers)
-      uint32_t kst = 0, kround = 0, vst = 0, vround = 0;
-      uint32_t q_round = 0;
-      uint32_t rot_round[2] = {0u, 0u};  // fused RoPE: rotated Q phases awaited per Q buffer
+      uint32_t k_t = 0, v_t = 0;       // KV tiles whose K / V this issuer has consumed
       uint32_t p_round[2] = {0u, 0u}, o_round[2] = {0u, 0u};
       bool o_pending[2] = {false, false};  // an epilogue of tile i has not been waited for
       bool ok = true;
+      // K(t) is ring load 2t, V(t) ring load 2t + 1; load p sits in slot
+      // p % NKV, and the phase of its full barrier has parity (p / NKV) & 1
+      auto k_slot = [&]() -> uint32_t { return (2u * k_t) % NKV; };
+      auto k_par = [&]() -> uint32_t { return ((2u * k_t) / NKV) & 1u; };
+      auto v_slot = [&]() -> uint32_t { return (2u * v_t + 1u) % NKV; };
+      auto v_par = [&]() -> uint32_t { return ((2u * v_t + 1u) / NKV) & 1u; };
 
-      auto next_flags = [&](int& flags) -> bool {
+      auto next_flags = [&](int& flags, int& qseq) -> bool {
         if (!sy.warp(kMFull + mslot, mround & 1)) return false;
         flags = *reinterpret_cast<volatile int*>(&meta[mslot].flags);
+        qseq = *reinterpret_cast<volatile int*>(&meta[mslot].qseq);
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kMEmpty + mslot]);
         if (++mslot == kMetaSlots) {
@@ -805,13 +840,13 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       // constant to the start-address field (14 bits of addr >> 4, which no
       // offset inside the tile can overflow).
       const uint64_t q_desc0 = sdesc_sw128(q_addr, 16, 1024);
-      const uint64_t k_desc0 = sdesc_sw128(k_addr, 16, 1024);
-      const uint64_t v_desc0 = sdesc_sw128(v_addr, BN * 128, 1024);
-      // S_i = Q_i K^T for the K tile in stage kst, Q buffer qb, into S buffer sb
+      const uint64_t k_desc0 = sdesc_sw128(kv_addr, 16, 1024);
+      const uint64_t v_desc0 = sdesc_sw128(kv_addr, BN * 128, 1024);
+      // S_i = Q_i K^T for the current K tile, Q tile buffer qb, into S buffer sb
       auto issue_s = [&](int i, uint32_t sb, uint32_t qb) {
         const uint32_t d_tmem = tmem_base + L::s_col(i, sb);
-        const uint64_t qd = q_desc0 + static_cast<uint64_t>((qb * QT + i) * (L::kQBytes >> 4));
-        const uint64_t kd = k_desc0 + static_cast<uint64_t>(kst * (L::kKBytes >> 4));
+        const uint64_t qd = q_desc0 + static_cast<uint64_t>(qb * (L::kQBytes >> 4));
+        const uint64_t kd = k_desc0 + static_cast<uint64_t>(k_slot() * (L::kKVBytes >> 4));
         constexpr int QC = (kTileM * 128) >> 4;  // next 64-column chunk of Q
         constexpr int KC = (BN * 128) >> 4;      // next 64-column chunk of K
         if constexpr (D == 128) {
@@ -821,11 +856,11 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
           umma_ss_group4<2, 2, 4, 4, 6, 6>(d_tmem, qd, kd, kIdescS, 0u);
         }
       };
-      // O_i (+)= P_i V for the V tile in stage vst, P_i in S buffer sb
+      // O_i (+)= P_i V for the current V tile, P_i in S buffer sb
       auto issue_pv = [&](int i, bool first, uint32_t sb) {
         const uint32_t d_tmem = tmem_base + 256 + i * 128;
         const uint32_t a_tmem = tmem_base + L::s_col(i, sb);
-        const uint64_t vd = v_desc0 + static_cast<uint64_t>(vst * (L::kVBytes >> 4));
+        const uint64_t vd = v_desc0 + static_cast<uint64_t>(v_slot() * (L::kKVBytes >> 4));
         constexpr int VS = (16 * 128) >> 4;  // 16 rows of V per K=16 step
         if constexpr (BN == 128) {
           umma_ts_group8<VS>(d_tmem, a_tmem, vd, kIdescO, first ? 0u : 1u);
@@ -833,18 +868,8 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
           umma_ts_group4<VS>(d_tmem, a_tmem, vd, kIdescO, first ? 0u : 1u);
         }
       };
-      auto advance_k = [&]() {
-        if (++kst == kStages) {
-          kst = 0;
-          ++kround;
-        }
-      };
-      auto advance_v = [&]() {
-        if (++vst == kStages) {
-          vst = 0;
-          ++vround;
-        }
-      };
+      auto advance_k = [&]() { ++k_t; };
+      auto advance_v = [&]() { ++v_t; };
       auto wait_o_empty = [&](int i, bool first) -> bool {
         if (first && o_pending[i]) {
           if (!sy.warp(kOEmpty + i, o_round[i] & 1)) return false;
@@ -854,7 +879,11 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         return true;
       };
 
-      if constexpr (kBufs<BN, QT> == 2) {
+      if constexpr (kSBufs<BN, QT> == 2) {
+        // The S stream fetches K(t+2) before PV(t) is issued, so K(t+2) must
+        // not need V(t)'s slot: four slots (K and V alternate between two
+        // pairs of them).
+        static_assert(kKVSlots<BN> == 4, "two S buffers need four K/V slots");
         // Two S buffers per Q tile (i = me: this issuer's tile).  The S
         // stream runs two KV tiles ahead of the PV stream: for each tile t,
         // PV_i(t) is followed by S_i(t+2),
@@ -862,7 +891,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         // thread run in issue order), so the softmax of tile t+1 never waits
         // for the MMAs of tile t.  Every buffer has its own S-full and P-full
         // barrier: a warpgroup may finish P(t+1) before P(t) is waited for.
-        uint32_t q_seq = 0, qb = 0;             // items the S stream entered; its Q buffer
+        uint32_t qb = 0, qpar = 0;  // this issuer's Q tile of the S stream's item: buffer, parity
         uint32_t s_cnt[2] = {0u, 0u};           // S_i issued (buffer = s_cnt & 1)
         uint32_t pv_cnt[2] = {0u, 0u};          // PV_i issued (buffer = pv_cnt & 1)
         uint32_t fq = 0u;  // 4-bit flags of the (at most four) tiles with S issued, PV not yet
@@ -872,31 +901,34 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         // next tile of the S stream: its metadata, its item's Q buffer (first
         // tile of an item) and its K tile
         auto s_fetch = [&](int& flags) -> bool {
-          if (!next_flags(flags)) return false;
+          int qseq = 0;
+          if (!next_flags(flags, qseq)) return false;
           if (flags & kStop) {
             s_end = true;
             return true;
           }
           if (flags & kFirst) {
-            qb = q_seq & 1u;
-            if constexpr (ROPE) {
-              // the rotated Q is awaited right before the first S MMA: the
-              // softmax rotates it only after its last P of the previous item
-              rot_wait = true;
-            } else {
-              if (!sy.warp(kQFull + qb, (q_seq >> 1) & 1u)) return false;
+            const uint32_t u = static_cast<uint32_t>(qseq) + static_cast<uint32_t>(me);
+            qb = u % NQ;
+            qpar = (u / NQ) & 1u;
+            if (me == 0 || (flags & kHasQ1)) {
+              if constexpr (ROPE) {
+                // the rotated Q is awaited right before the first S MMA: the
+                // softmax rotates it only after its last P of the previous item
+                rot_wait = true;
+              } else {
+                if (!sy.warp(kQFull + qb, qpar)) return false;
+              }
             }
-            ++q_seq;
           }
-          if (!sy.warp(kKFull + kst, kround & 1)) return false;
+          if (!sy.warp(kKVFull + k_slot(), k_par())) return false;
           tc_fence_after();
           return true;
         };
         auto s_one = [&](int i) -> bool {
           if constexpr (ROPE) {
             if (rot_wait) {
-              if (!sy.warp(kQRot + 2 * i + qb, rot_round[qb] & 1u)) return false;
-              ++rot_round[qb];
+              if (!sy.warp(kQRot + qb, qpar)) return false;
               rot_wait = false;
               tc_fence_after();
             }
@@ -909,8 +941,9 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         };
         auto s_done = [&](int flags) {
           rot_wait = false;
-          umma_commit_elect(&bars[kKEmpty + kst]);
-          if (flags & kLast) umma_commit_elect(&bars[kQEmpty + qb]);
+          umma_commit_elect(&bars[kKVEmpty + k_slot()]);
+          if ((flags & kLast) && (me == 0 || (flags & kHasQ1)))
+            umma_commit_elect(&bars[kQEmpty + qb]);
           advance_k();
           const uint32_t sh = (n_s & 3u) * 4u;
           fq = (fq & ~(0xFu << sh)) | (static_cast<uint32_t>(flags & 0xF) << sh);
@@ -939,7 +972,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
             if (!s_fetch(nxt)) { ok = false; break; }
             ahead = !s_end;
           }
-          if (!sy.warp(kVFull + vst, vround & 1)) { ok = false; break; }
+          if (!sy.warp(kKVFull + v_slot(), v_par())) { ok = false; break; }
           {
             const int i = me;
             if (i == 0 || (cur & kHasQ1)) {
@@ -954,7 +987,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
             }
             if (ahead && (i == 0 || (nxt & kHasQ1)) && !s_one(i)) { ok = false; break; }
           }
-          umma_commit_elect(&bars[kVEmpty + vst]);
+          umma_commit_elect(&bars[kKVEmpty + v_slot()]);
           advance_v();
           if (ahead) s_done(nxt);
           ++n_pv;
@@ -982,41 +1015,44 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
             if (lane == 0) mbar_arrive(&bars[kTurn + (me ^ 1)]);
           }
         };
+        uint32_t my_qb = 0;  // Q tile buffer of this issuer's tile in the current item
         // S MMAs (all BN key columns) of the first tile of an item
-        auto start_item = [&](int flags) -> bool {
-          if constexpr (ROPE) {
-            if (me == 0 || (flags & kHasQ1)) {
-              if (!sy.warp(kQRot + 2 * me, rot_round[0] & 1)) return false;
-              ++rot_round[0];
+        auto start_item = [&](int flags, int qseq) -> bool {
+          const uint32_t u = static_cast<uint32_t>(qseq) + static_cast<uint32_t>(me);
+          my_qb = u % NQ;
+          const uint32_t qpar = (u / NQ) & 1u;
+          const bool mine = me == 0 || (flags & kHasQ1);
+          if (mine) {
+            if constexpr (ROPE) {
+              if (!sy.warp(kQRot + my_qb, qpar)) return false;
+            } else {
+              if (!sy.warp(kQFull + my_qb, qpar)) return false;
             }
-          } else {
-            if (!sy.warp(kQFull, q_round & 1)) return false;
-            ++q_round;
           }
-          if (!sy.warp(kKFull + kst, kround & 1)) return false;
+          if (!sy.warp(kKVFull + k_slot(), k_par())) return false;
           tc_fence_after();
           if (!take_turn()) return false;
-          if (me == 0 || (flags & kHasQ1)) {
-            issue_s(me, 0u, 0u);
+          if (mine) {
+            issue_s(me, 0u, my_qb);
             umma_commit_elect(&bars[kSFull + 2 * me]);
           }
           pass_turn();
-          umma_commit_elect(&bars[kKEmpty + kst]);
-          if (flags & kLast) umma_commit_elect(&bars[kQEmpty]);
+          umma_commit_elect(&bars[kKVEmpty + k_slot()]);
+          if ((flags & kLast) && mine) umma_commit_elect(&bars[kQEmpty + my_qb]);
           advance_k();
           return true;
         };
-        int cur = 0;
-        ok = next_flags(cur);
-        if (ok && !(cur & kStop)) ok = start_item(cur);
+        int cur = 0, cur_qseq = 0;
+        ok = next_flags(cur, cur_qseq);
+        if (ok && !(cur & kStop)) ok = start_item(cur, cur_qseq);
         while (ok && !(cur & kStop)) {
           const bool first = (cur & kFirst) != 0;
           const bool last = (cur & kLast) != 0;
           const bool q1 = (cur & kHasQ1) != 0;
           int nxt = 0;
-          if (!sy.warp(kVFull + vst, vround & 1)) { ok = false; break; }
+          if (!sy.warp(kKVFull + v_slot(), v_par())) { ok = false; break; }
           if (!last) {
-            if (!sy.warp(kKFull + kst, kround & 1)) { ok = false; break; }
+            if (!sy.warp(kKVFull + k_slot(), k_par())) { ok = false; break; }
             tc_fence_after();
             // the metadata of this K tile was written before its load was armed
             nxt = *reinterpret_cast<volatile int*>(&meta[mslot].flags);
@@ -1044,21 +1080,22 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
               umma_commit_elect(&bars[kOFull + i]);
               o_pending[i] = true;
             } else {
-              issue_s(i, 0u, 0u);
+              issue_s(i, 0u, my_qb);
               umma_commit_elect(&bars[kSFull + 2 * i]);
             }
             pass_turn();
           }
-          umma_commit_elect(&bars[kVEmpty + vst]);
+          umma_commit_elect(&bars[kKVEmpty + v_slot()]);
           advance_v();
           if (!last) {
-            umma_commit_elect(&bars[kKEmpty + kst]);
-            if (nxt & kLast) umma_commit_elect(&bars[kQEmpty]);
+            umma_commit_elect(&bars[kKVEmpty + k_slot()]);
+            if ((nxt & kLast) && (me == 0 || q1)) umma_commit_elect(&bars[kQEmpty + my_qb]);
             advance_k();
           } else {
-            if (!next_flags(nxt)) { ok = false; break; }
+            int nq = 0;
+            if (!next_flags(nxt, nq)) { ok = false; break; }
             if (nxt & kStop) break;
-            if (!start_item(nxt)) { ok = false; break; }
+            if (!start_item(nxt, nq)) { ok = false; break; }
           }
           cur = nxt;
         }
@@ -1157,8 +1194,8 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p, const Rop
     uint32_t n_tiles = 0, o_round = 0;  // KV tiles of this warpgroup so far; epilogues
     float m_run = -CUDART_INF_F, l_run = 0.f;
     int rt0 = 0, rt1 = 0, h = 0;
-    uint32_t q_items = 0, item_qb = 0, item_qpar = 0;  // items seen; Q buffer and parity of this one
-    uint32_t rot_cnt[2] = {0u, 0u};  // fused RoPE: Q tiles this warpgroup rotated, per Q buffer
+    constexpr uint32_t NQ = kQSlots<BN>;
+    uint32_t item_qb = 0, item_qpar = 0;  // fused RoPE: Q tile buffer of this item, its parity
 
     // Epilogue of an item: once its last PV is done, O / l -> bf16 out rows
     // (guarded: rows from e_rt1 on belong to the next sample) and lse.
@@ -1209,10 +1246,12 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p, const Rop
         const int row_elems = p.hq * D;
         const uint32_t my_row = stage + static_cast<uint32_t>(lane) * 64u;
         const uint32_t my_sw = static_cast<uint32_t>((lane >> 1) & 3);
+        // the whole O row with one TMEM load and one wait (the S row is dead)
+        uint32_t orow[D];
+        tmem_ld_row<D>(o_tmem, orow);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(o_tmem + c * 32, rr);
+          const uint32_t* rr = orow + c * 32;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             st_shared_v4(my_row + ((static_cast<uint32_t>(u) ^ my_sw) << 4),
@@ -1259,7 +1298,7 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p, const Rop
       if (!epi_pending) return true;
       epi_pending = false;
       const uint32_t lt = n_tiles - 1u;
-      if constexpr (kBufs<BN, QT> == 2)
+      if constexpr (kSBufs<BN, QT> == 2)
         return epilogue(rt0 + row, rt1, h, m_run, l_run, kPVDone + 2 * wg + (lt & 1u),
                         (lt >> 1) & 1u);
       else
@@ -1288,9 +1327,13 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p, const Rop
         n_h = mb.w;
         n_rt0 = mb.y + wg * BM;
         n_rt1 = min(n_rt0 + BM, mb.z);
-        item_qb = q_items % kBufs<BN, QT>;
-        item_qpar = (q_items / kBufs<BN, QT>) & 1u;
-        ++q_items;
+        if constexpr (ROPE) {
+          // the Q ring position of this warpgroup's tile (read before the
+          // slot is released below)
+          const uint32_t u = static_cast<uint32_t>(meta[mslot].qseq) + static_cast<uint32_t>(wg);
+          item_qb = u % NQ;
+          item_qpar = (u / NQ) & 1u;
+        }
         if constexpr (!ROPE) {
           h = n_h;
           rt0 = n_rt0;
@@ -1315,19 +1358,21 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p, const Rop
           // this warpgroup's Q tile of the item: rotate it in place once it
           // has landed, then hand it to the tensor cores
           const int a_start = meta[cur_slot].a;
-          const uint32_t qtile = smem_u32(smem + L::kQ + (item_qb * QT + wg) * L::kQBytes);
+          const uint32_t qtile = smem_u32(smem + L::kQ + item_qb * L::kQBytes);
           if (!sy.warp(kQFull + item_qb, item_qpar)) break;
           rope_q_tile_row<D>(ra, qtile, row, static_cast<float>(max(n_rt0 + row - a_start, 0)));
           fence_proxy_async_smem();
-          const int rb = kQRot + 2 * wg + static_cast<int>(item_qb);
+          const int rb = kQRot + static_cast<int>(item_qb);
           mbar_arrive(&bars[rb]);
           if (ra.q_rot != nullptr) {
             // every row of the tile is rotated once the phase completes; the
-            // tile stays in place until this item's last S MMA is done
-            if (!sy.warp(rb, rot_cnt[item_qb] & 1u)) break;
+            // buffer is refilled only after the arrival below
+            if (!sy.warp(rb, item_qpar)) break;
             store_q_tile<D, IdxT>(p, ra, qtile, row, n_rt1 - n_rt0, n_rt0, n_h);
           }
-          ++rot_cnt[item_qb];
+          // this thread is done with the buffer (the issuer's commit after the
+          // item's last S MMA completes its empty phase)
+          mbar_arrive(&bars[kQEmpty + item_qb]);
           if constexpr (kDefer) {
             if (!flush_epilogue()) break;
           }
@@ -1411,8 +1456,8 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p, const Rop
       if (lane == 0) mbar_arrive(&bars[kMEmpty + cur_slot]);
 
       // S buffer of this tile and the parity of its S-full / P-full phase
-      const uint32_t sb = n_tiles % kBufs<BN, QT>;
-      const uint32_t spar = (n_tiles / kBufs<BN, QT>) & 1u;
+      const uint32_t sb = n_tiles % kSBufs<BN, QT>;
+      const uint32_t spar = (n_tiles / kSBufs<BN, QT>) & 1u;
       const uint32_t s_cur = tmem_base + lane_addr + L::s_col(wg, sb);
       if (!sy.warp(kSFull + 2 * wg + sb, spar)) break;
       tc_fence_after();
@@ -1461,7 +1506,7 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p, const Rop
           // that PV here.  Its done barrier belongs to its S buffer; the
           // barrier's previous phase (the PV two tiles back) completed before
           // this tile's S, so the parity is exact.
-          if constexpr (kBufs<BN, QT> == 2) {
+          if constexpr (kSBufs<BN, QT> == 2) {
             const uint32_t pt = n_tiles - 1u;
             o_ok = sy.warp(kPVDone + 2 * wg + (pt & 1u), (pt >> 1) & 1u);
             tc_fence_after();
@@ -1507,7 +1552,7 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p, const Rop
         // issue order, so every earlier PV is done too)
         int wbar;
         uint32_t wpar;
-        if constexpr (kBufs<BN, QT> == 2) {
+        if constexpr (kSBufs<BN, QT> == 2) {
           wbar = kPVDone + 2 * wg + sb;
           wpar = spar;
         } else {
