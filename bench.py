@@ -13,7 +13,7 @@ Metric: effective attention TFLOP/s, counting 4 * head_dim FLOPs per unmasked
 reported as achieved HBM GB/s (read + write of q and k).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--configs all|headline]
+                    [--configs all|headline|1..5]
     python bench.py --sweep sparsity [--sweep-tokens T]
 
 The sparsity sweep (FlashMask article, section 4.3) times the attention call
@@ -542,7 +542,12 @@ def run_ours(args):
     flush = L2Flush(torch, device)
     traffic = stored_traffic()
 
-    cfgs = [HEADLINE_CFG] if args.configs == "headline" else [1, 2, 3, 4, 5]
+    if args.configs == "all":
+        cfgs = [1, 2, 3, 4, 5]
+    elif args.configs == "headline":
+        cfgs = [HEADLINE_CFG]
+    else:  # one workload (for profiling) in per_config, then the headline's timed region
+        cfgs = [int(args.configs)]
     per_config = {}
     # the other workloads first (short runs), then the headline's timed region
     for cfg in cfgs:
@@ -919,7 +924,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--configs", choices=["all", "headline"], default="all")
+    ap.add_argument("--configs", choices=["all", "headline", "1", "2", "3", "4", "5"],
+                    default="all")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--min-warmup-seconds", type=float, default=1.0)
