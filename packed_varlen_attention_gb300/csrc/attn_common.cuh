@@ -270,14 +270,6 @@ __device__ __forceinline__ void umma_ts_group8(uint32_t d_tmem, uint32_t a_tmem,
                : "memory");
 }
 
-// Pull a tile into L2 ahead of its TMA load (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
 // Bounded waits shared by every role; on expiry the CTA is told to stop and
 // FM_DEVERR_TIMEOUT is recorded.
 

@@ -67,18 +67,16 @@ constexpr int kMetaSlots = 4;
 // Interval-masked tiles whose columns form at most this many runs of equal
 // (LTS, LTE, UTS, UTE) get a run table instead of per-column tests.
 constexpr int kMaxRuns = 8;
-constexpr int kPrefetchAhead = 3;  // K/V tiles pulled into L2 ahead of their loads
 
 // Shared-memory rings.  K and V tiles share one ring of kKVSlots slots,
 // loaded in the order K(0), V(0), K(1), V(1), ... of the CTA's KV tiles
-// (load p into slot p mod kKVSlots): with three slots, K(t+2) takes the slot
-// V(t) leaves once the PV MMAs of tile t are done, one KV step before S(t+2)
-// needs it.  Q tiles have their own ring of kQSlots tile buffers, filled in
-// work order (tile 0, then tile 1 of each item), so the next item's first Q
-// tile lands while the current item still runs and its second one as soon
-// as the current item's tile 0 has had its last S MMA.  Three K/V slots and
-// three Q tiles of 32 KB take the shared memory that two K stages, two V
-// stages and one pair of Q tiles took before.
+// (load p into slot p mod kKVSlots): with four slots K(t+2) takes the slot
+// K(t) leaves once the S MMAs of tile t are done, and V(t+2) the one V(t)
+// leaves after the PV MMAs of tile t.  Q tiles have their own ring of
+// kQSlots tile buffers, filled in work order (tile 0, then tile 1 of each
+// item); a buffer is reloaded once the tile held there before has had its
+// last S MMA, so with two buffers the next item's tile 0 loads while the
+// current item's tile 1 still runs its last KV step.
 template <int BN>
 constexpr int kKVSlots = 4;
 template <int BN>
@@ -659,24 +657,23 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         continue;
       }
 
-      // pass 2: metadata and K for every tile live for either Q tile
+      // The item's Q tile 0 goes first, as soon as its buffer is free (the
+      // tile held there before has had its last S MMA): nothing between the
+      // classification and this load depends on it.
+      if (!load_q(q_seq, h, r0)) {
+        ok = false;
+        break;
+      }
+
+      // pass 2: metadata and K for every tile live for either Q tile.  No
+      // K/V tile is prefetched into L2 ahead of its load: with such
+      // prefetches (two or three tiles ahead) the kernel measured 2-8 %
+      // slower.
       int pushed = 0;
       for (int base = 0; base < kt_end && ok; base += 32) {
         int my0, my1;
         tile_classes<BN>(p, mh, s, a, b, r0, r1, r2, base + lane, kt_end, my0, my1);
         uint32_t live = __ballot_sync(0xffffffffu, my0 != kClsF || my1 != kClsF);
-        if (lane == 0) {
-          // the first live tiles of the chunk (the very first is loaded next)
-          uint32_t m = live & (live - 1u);
-          for (int t = 1; t < kPrefetchAhead && m != 0u; ++t, m &= m - 1u) {
-            const int ca = a + (base + __ffs(m) - 1) * BN;
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-              tma_prefetch_l2(&tk, kvh * D + c * 64, ca);
-              tma_prefetch_l2(&tv, kvh * D + c * 64, ca);
-            }
-          }
-        }
         while (live != 0u) {
           const int l = __ffs(live) - 1;
           live &= live - 1u;
@@ -684,20 +681,6 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
           const int cls1 = __shfl_sync(0xffffffffu, my1, l);
           const int c0 = a + (base + l) * BN;
           const int c1 = min(c0 + BN, b);
-          if (lane == 0) {
-            // warm L2 with the K/V tile kPrefetchAhead live tiles further on
-            // (within this 32-tile chunk); its TMA load then hits L2
-            uint32_t m = live;
-            for (int t = 1; t < kPrefetchAhead && m != 0u; ++t) m &= m - 1u;
-            if (m != 0u) {
-              const int ca = a + (base + __ffs(m) - 1) * BN;
-#pragma unroll
-              for (int c = 0; c < D / 64; ++c) {
-                tma_prefetch_l2(&tk, kvh * D + c * 64, ca);
-                tma_prefetch_l2(&tv, kvh * D + c * 64, ca);
-              }
-            }
-          }
           const int flags = (pushed == 0 ? kFirst : 0) | (pushed == n_live - 1 ? kLast : 0) |
                             (has_q1 ? kHasQ1 : 0);
           const bool copy = (cls0 == kClsP || cls1 == kClsP) && p.sri != nullptr;
@@ -705,13 +688,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
             ok = false;
             break;
           }
-          // the item's Q tile 0 first (its buffer was freed long before), then
-          // K of the first tile, then Q tile 1, whose buffer frees when the
-          // previous item's tile 0 has had its last S MMA
-          if (pushed == 0 && !load_q(q_seq, h, r0)) {
-            ok = false;
-            break;
-          }
+          // K of the tile; after the item's first K, its Q tile 1
           {
             const uint32_t pos = 2u * kv_t;  // K(t): even ring loads
             const uint32_t slot = pos % NKV;
