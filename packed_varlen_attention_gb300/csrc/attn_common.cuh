@@ -298,6 +298,21 @@ __device__ __forceinline__ float sum_f32x2(uint64_t v) {
   return lo + hi;
 }
 
+// (lo * s, hi * s) rounded to bf16x2 (lo in the low half) with one packed
+// multiply; s2 holds s in both halves.  Bitwise the same as two scalar
+// round-to-nearest multiplies followed by the conversion.
+__device__ __forceinline__ uint32_t scale_pack_bf16x2(uint32_t lo, uint32_t hi, uint64_t s2) {
+  uint32_t packed;
+  asm("{\n\t.reg .b64 x, y;\n\t.reg .f32 y0, y1;\n\t"
+      "mov.b64 x, {%1, %2};\n\t"
+      "mul.rn.f32x2 y, x, %3;\n\t"
+      "mov.b64 {y0, y1}, y;\n\t"
+      "cvt.rn.bf16x2.f32 %0, y1, y0;\n\t}"
+      : "=r"(packed)
+      : "r"(lo), "r"(hi), "l"(s2));
+  return packed;
+}
+
 // Two softmax numerators at once: p_k = 2^(s_k * scale + base) with one
 // packed FMA and two ex2; (p0, p1) is added to the packed partial sums and
 // returned as bf16x2 (p0 in the low half).

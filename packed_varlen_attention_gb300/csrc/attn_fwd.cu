@@ -1190,6 +1190,7 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p, const Rop
           smem_u32(smem + L::kStage) +
           static_cast<uint32_t>(((threadIdx.x >> 5) - kFirstSoftmaxWarp) * L::kStageBytesPerWarp);
       const float inv_l = (e_l > 0.f) ? 1.f / e_l : 0.f;
+      const uint64_t inv_l2 = pack_f32x2(inv_l, inv_l);
       if constexpr (sizeof(IdxT) == 8) {
         // 64-bit indexing: each thread stores its own row (the staged
         // variant below costs this instantiation registers in the S loop)
@@ -1203,15 +1204,10 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p, const Rop
             uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              d4[u] = make_uint4(
-                  pack_bf16x2(__uint_as_float(rr[8 * u + 0]) * inv_l,
-                              __uint_as_float(rr[8 * u + 1]) * inv_l),
-                  pack_bf16x2(__uint_as_float(rr[8 * u + 2]) * inv_l,
-                              __uint_as_float(rr[8 * u + 3]) * inv_l),
-                  pack_bf16x2(__uint_as_float(rr[8 * u + 4]) * inv_l,
-                              __uint_as_float(rr[8 * u + 5]) * inv_l),
-                  pack_bf16x2(__uint_as_float(rr[8 * u + 6]) * inv_l,
-                              __uint_as_float(rr[8 * u + 7]) * inv_l));
+              d4[u] = make_uint4(scale_pack_bf16x2(rr[8 * u + 0], rr[8 * u + 1], inv_l2),
+                                 scale_pack_bf16x2(rr[8 * u + 2], rr[8 * u + 3], inv_l2),
+                                 scale_pack_bf16x2(rr[8 * u + 4], rr[8 * u + 5], inv_l2),
+                                 scale_pack_bf16x2(rr[8 * u + 6], rr[8 * u + 7], inv_l2));
             }
           }
         }
@@ -1232,14 +1228,10 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p, const Rop
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             st_shared_v4(my_row + ((static_cast<uint32_t>(u) ^ my_sw) << 4),
-                         pack_bf16x2(__uint_as_float(rr[8 * u + 0]) * inv_l,
-                                     __uint_as_float(rr[8 * u + 1]) * inv_l),
-                         pack_bf16x2(__uint_as_float(rr[8 * u + 2]) * inv_l,
-                                     __uint_as_float(rr[8 * u + 3]) * inv_l),
-                         pack_bf16x2(__uint_as_float(rr[8 * u + 4]) * inv_l,
-                                     __uint_as_float(rr[8 * u + 5]) * inv_l),
-                         pack_bf16x2(__uint_as_float(rr[8 * u + 6]) * inv_l,
-                                     __uint_as_float(rr[8 * u + 7]) * inv_l));
+                         scale_pack_bf16x2(rr[8 * u + 0], rr[8 * u + 1], inv_l2),
+                         scale_pack_bf16x2(rr[8 * u + 2], rr[8 * u + 3], inv_l2),
+                         scale_pack_bf16x2(rr[8 * u + 4], rr[8 * u + 5], inv_l2),
+                         scale_pack_bf16x2(rr[8 * u + 6], rr[8 * u + 7], inv_l2));
           }
           __syncwarp();
 #pragma unroll
