@@ -1054,6 +1054,7 @@ __device__ __forceinline__ void bwd_elementwise_role(const AttnBwdParams& p) {
       const uint32_t acc_t = tmem_base + lane_addr +
                              (Mode == kModeDQ ? L::kAcc0 + wg * (D / 2)
                                               : (wg == 0 ? L::kAcc0 : L::kAcc1));
+      const uint64_t f2 = pack_f32x2(f, f);
 #pragma unroll
       for (int c = 0; c < kCols / 32; ++c) {
         uint32_t rr[32];
@@ -1062,14 +1063,10 @@ __device__ __forceinline__ void bwd_elementwise_role(const AttnBwdParams& p) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            d4[u] = make_uint4(pack_bf16x2(__uint_as_float(rr[8 * u + 0]) * f,
-                                           __uint_as_float(rr[8 * u + 1]) * f),
-                               pack_bf16x2(__uint_as_float(rr[8 * u + 2]) * f,
-                                           __uint_as_float(rr[8 * u + 3]) * f),
-                               pack_bf16x2(__uint_as_float(rr[8 * u + 4]) * f,
-                                           __uint_as_float(rr[8 * u + 5]) * f),
-                               pack_bf16x2(__uint_as_float(rr[8 * u + 6]) * f,
-                                           __uint_as_float(rr[8 * u + 7]) * f));
+            d4[u] = make_uint4(scale_pack_bf16x2(rr[8 * u + 0], rr[8 * u + 1], f2),
+                               scale_pack_bf16x2(rr[8 * u + 2], rr[8 * u + 3], f2),
+                               scale_pack_bf16x2(rr[8 * u + 4], rr[8 * u + 5], f2),
+                               scale_pack_bf16x2(rr[8 * u + 6], rr[8 * u + 7], f2));
           }
         }
       }
