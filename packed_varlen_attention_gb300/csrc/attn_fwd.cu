@@ -1191,27 +1191,7 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p, const Rop
           static_cast<uint32_t>(((threadIdx.x >> 5) - kFirstSoftmaxWarp) * L::kStageBytesPerWarp);
       const float inv_l = (e_l > 0.f) ? 1.f / e_l : 0.f;
       const uint64_t inv_l2 = pack_f32x2(inv_l, inv_l);
-      if constexpr (sizeof(IdxT) == 8) {
-        // 64-bit indexing: each thread stores its own row (the staged
-        // variant below costs this instantiation registers in the S loop)
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
-                             (static_cast<IdxT>(e_r) * p.hq + e_h) * static_cast<IdxT>(D);
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(o_tmem + c * 32, rr);
-          if (e_r < e_rt1) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              d4[u] = make_uint4(scale_pack_bf16x2(rr[8 * u + 0], rr[8 * u + 1], inv_l2),
-                                 scale_pack_bf16x2(rr[8 * u + 2], rr[8 * u + 3], inv_l2),
-                                 scale_pack_bf16x2(rr[8 * u + 4], rr[8 * u + 5], inv_l2),
-                                 scale_pack_bf16x2(rr[8 * u + 6], rr[8 * u + 7], inv_l2));
-            }
-          }
-        }
-      } else {
+      {
         const int tok0 = e_r - lane;  // token of this warp's first row
         // rows of this warp: one 64-bit base, 32-bit offsets (32 * Hq * D fits)
         __nv_bfloat16* const dst0 = static_cast<__nv_bfloat16*>(p.out) +
