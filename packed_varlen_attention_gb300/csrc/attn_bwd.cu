@@ -221,6 +221,22 @@ __device__ __forceinline__ int dkv_class(const AttnBwdParams& p, const ResTile& 
   return classify_block(q0, q1, rt.r0, rt.r1, st, p.sri != nullptr, p.causal != 0);
 }
 
+// Steps of the dK/dV item of tile rt under mask head mh: its 64-row Q tiles
+// that are not fully masked.
+__device__ __forceinline__ int dkv_tile_steps(const AttnBwdParams& p, const ResTile& rt, int mh) {
+  const int q_first = dkv_q_first(p, rt);
+  const int n_q = (rt.b - rt.a + kSub - 1) / kSub - q_first;
+  int st[8];
+  if (p.sri != nullptr) load_stats(p, mh, static_cast<int64_t>(rt.a / kStatTile) + rt.s + rt.t, st);
+  int n = 0;
+  for (int k = 0; k < n_q; ++k) {
+    const int q0 = rt.a + (q_first + k) * kSub;
+    const int q1 = min(q0 + kSub, rt.b);
+    n += classify_block(q0, q1, rt.r0, rt.r1, st, p.sri != nullptr, p.causal != 0) != kClsF;
+  }
+  return n;
+}
+
 // P and dS for two elements: p = 2^(x * c + nl), ds = p * (y + nd); returns
 // both as bf16x2 (first element in the low half).
 __device__ __forceinline__ void bwd_pair(uint32_t x0, uint32_t x1, uint32_t y0, uint32_t y1,
@@ -332,11 +348,20 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const AttnBwdParams p) {
 // a sample stay together, dK/dV in tile order and dQ in reverse tile order,
 // so that under a causal mask the tiles with the most steps come first and
 // the concurrently running items of one sample share their streamed tiles in
-// L2.  Only real tiles are listed.
+// L2.  dK/dV items can be long (a key tile near the start of a long causal
+// sample walks every later Q tile of every q head of its group): when the
+// largest one exceeds half of the work per CTA, the sample order leaves a
+// tail of one CTA still on a large item, so the key tiles are ordered by
+// their own step counts instead, largest first (the costliest mask head's
+// count).  Only real tiles are listed.
 template <int Mode>
 __global__ void __launch_bounds__(kCostBins) bwd_plan_order_kernel(const AttnBwdParams p) {
   __shared__ int tiles_in_bin[kCostBins];
+  __shared__ int step_bin[kCostBins];  // dK/dV: key tiles per step count
   __shared__ int warp_tot[kCostBins / 32];
+  __shared__ unsigned long long steps_total;
+  __shared__ int steps_max;
+  __shared__ int by_steps;
   const int T = static_cast<int>(p.T);
   int* order = Mode == kModeDQ ? p.order_q : p.order_kv;
   pdl_trigger();
@@ -344,6 +369,11 @@ __global__ void __launch_bounds__(kCostBins) bwd_plan_order_kernel(const AttnBwd
   const int tid = threadIdx.x;
   const int lane = tid & 31, w = tid >> 5;
   tiles_in_bin[tid] = 0;
+  step_bin[tid] = 0;
+  if (tid == 0) {
+    steps_total = 0ull;
+    steps_max = 0;
+  }
   __syncthreads();
   auto n_tiles_of = [&](int s) -> int {
     const int a = clamp_tok(__ldg(p.cu + s), T);
@@ -354,7 +384,40 @@ __global__ void __launch_bounds__(kCostBins) bwd_plan_order_kernel(const AttnBwd
     const int n = n_tiles_of(s);
     if (n > 0) atomicAdd(&tiles_in_bin[min(n, kCostBins - 1)], n);
   }
+  const int n_mh = p.hm > 1 ? p.hm : 1;
+  auto kv_steps = [&](const ResTile& rt) -> int {
+    int c = 0;
+    for (int mh = 0; mh < n_mh; ++mh) c = max(c, dkv_tile_steps(p, rt, mh));
+    return c;
+  };
+  if (Mode == kModeDKV) {
+    unsigned long long my_total = 0ull;
+    int my_max = 0;
+    for (int64_t u = tid; u < p.n_res_slots; u += kCostBins) {
+      const ResTile rt = res_tile(p, u);
+      if (!rt.real) continue;
+      const int c = kv_steps(rt);
+      my_total += static_cast<unsigned long long>(c);
+      my_max = max(my_max, c);
+      atomicAdd(&step_bin[min(c, kCostBins - 1)], 1);
+    }
+    if (my_total != 0ull) atomicAdd(&steps_total, my_total);
+    if (my_max != 0) atomicMax(&steps_max, my_max);
+  }
   __syncthreads();
+  if (Mode == kModeDKV) {
+    // an item walks its key tile for every q head of the group: the largest
+    // item is group * max steps, the work per CTA Hq * total / CTAs
+    if (tid == 0) {
+      const unsigned long long group = static_cast<unsigned long long>(p.hq / p.hkv);
+      by_steps = 2ull * group * static_cast<unsigned long long>(steps_max) *
+                     static_cast<unsigned long long>(max(p.num_sms, 1)) >
+                 static_cast<unsigned long long>(p.hq) * steps_total;
+    }
+    __syncthreads();
+    if (by_steps) tiles_in_bin[tid] = step_bin[tid];
+    __syncthreads();
+  }
   // exclusive prefix over bins in descending order (position 0: largest bin)
   const int bin = kCostBins - 1 - tid;
   const int cnt = tiles_in_bin[bin];
@@ -393,6 +456,14 @@ __global__ void __launch_bounds__(kCostBins) bwd_plan_order_kernel(const AttnBwd
     }
   }
   __syncthreads();
+  if (Mode == kModeDKV && by_steps) {
+    for (int64_t u = tid; u < p.n_res_slots; u += kCostBins) {
+      const ResTile rt = res_tile(p, u);
+      if (rt.real)
+        order[atomicAdd(&tiles_in_bin[min(kv_steps(rt), kCostBins - 1)], 1)] = static_cast<int>(u);
+    }
+    return;
+  }
   for (int s = tid; s < p.n_seqs; s += kCostBins) {
     const int n = n_tiles_of(s);
     if (n == 0) continue;
@@ -1122,9 +1193,11 @@ cudaError_t launch_all(const AttnBwdParams& p, const BwdMaps& m, int num_sms,
   cudaError_t e = launch_pdl(bwd_prep_kernel<D, IdxT>, dim3(static_cast<unsigned>(blocks)),
                              dim3(256), 0, stream, p);
   if (e != cudaSuccess) return e;
-  e = launch_mode<D, kModeDKV, IdxT>(p, m.k128, m.v128, m.q64, m.do64, num_sms, stream);
+  AttnBwdParams pp = p;
+  pp.num_sms = num_sms;
+  e = launch_mode<D, kModeDKV, IdxT>(pp, m.k128, m.v128, m.q64, m.do64, num_sms, stream);
   if (e != cudaSuccess) return e;
-  return launch_mode<D, kModeDQ, IdxT>(p, m.q128, m.do128, m.k64, m.v64, num_sms, stream);
+  return launch_mode<D, kModeDQ, IdxT>(pp, m.q128, m.do128, m.k64, m.v64, num_sms, stream);
 }
 
 }  // namespace

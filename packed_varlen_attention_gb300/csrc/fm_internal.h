@@ -145,6 +145,7 @@ struct AttnBwdParams {
   float scale;
   float scale_log2;
   uint64_t timeout_ns;
+  int num_sms;  // CTAs of the persistent passes (the planner's balance test)
 };
 
 // Tensor maps of the backward pass: 128-row and 64-row boxes of q, k, v, dout.
