@@ -223,6 +223,28 @@ __device__ __forceinline__ int kv_tiles_to_scan(const AttnParams& p, int a, int 
 // planner: work unit = (sample, pair of consecutive Q tiles)
 // ---------------------------------------------------------------------------
 
+// Rows of item `pair` of the sample [a, b): Q tile 0 [r0, r1), Q tile 1
+// [r1, r2) (empty when r2 == r1).  With QT = 2 and an odd number of Q tiles
+// the sample's first tile is the one without a partner: items pair tiles
+// (1, 2), (3, 4), ... from the back, so under a causal mask the tile that
+// runs with one warpgroup only is the cheapest one, not the costliest.
+template <int QT>
+__device__ __forceinline__ void item_rows(int a, int b, int64_t pair, int bm, int& r0, int& r1,
+                                          int& r2) {
+  int64_t t0 = pair * QT;  // first Q tile of the item
+  bool single = QT == 1;
+  if constexpr (QT == 2) {
+    const int64_t n_t = (static_cast<int64_t>(b) - a + bm - 1) / bm;
+    if (n_t & 1) {
+      single = pair == 0;
+      t0 = pair == 0 ? 0 : 2 * pair - 1;
+    }
+  }
+  r0 = static_cast<int>(min(static_cast<int64_t>(a) + t0 * bm, static_cast<int64_t>(b)));
+  r1 = min(r0 + bm, b);
+  r2 = single ? r1 : min(r0 + 2 * bm, b);
+}
+
 // The planner is two programmatic dependent launches (see launch_pdl): each
 // waits for the kernel before it, then lets the next one start launching,
 // so the attention kernel's set-up overlaps the planner.  Neither needs the
@@ -255,9 +277,8 @@ __global__ void __launch_bounds__(256) plan_cost_kernel(const AttnParams p) {
     if (lane == 0) p.cost[u] = -1;
     return;
   }
-  const int r0 = a + static_cast<int>(pair) * BM2;
-  const int r1 = min(r0 + p.block_m, b);
-  const int r2 = min(r0 + BM2, b);
+  int r0, r1, r2;
+  item_rows<QT>(a, b, pair, p.block_m, r0, r1, r2);
   const int kt_end = kv_tiles_to_scan<BN>(p, a, b, r2);
   // With one mask per q head the pair's items differ in cost; the order
   // uses the costliest head's count (all heads of a pair run side by side).
@@ -597,9 +618,8 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       const int mh = p.hm > 1 ? h : 0;
       const int a = clamp_tok(__ldg(p.cu + s), T);
       const int b = max(a, clamp_tok(__ldg(p.cu + s + 1), T));
-      const int r0 = min(a + pi.y * QT * BM, b);
-      const int r1 = min(r0 + BM, b);
-      const int r2 = min(r0 + QT * BM, b);
+      int r0, r1, r2;
+      item_rows<QT>(a, b, pi.y, BM, r0, r1, r2);
       const bool has_q1 = r2 > r1;  // (never with one Q tile per item)
       const int n_kv = (b - a + BN - 1) / BN;
       const int kt_end = (r2 > r0) ? kv_tiles_to_scan<BN>(p, a, b, r2) : 0;
