@@ -61,10 +61,13 @@ typedef enum fm_status {
 
 /* Bits of the device error word. */
 #define FM_DEVERR_TIMEOUT 0x1u /* a pipeline wait exceeded its limit      */
-#define FM_DEVERR_DATA 0x2u    /* malformed cu_seqlens seen on the device  */
+#define FM_DEVERR_DATA 0x2u    /* malformed cu_seqlens seen on the device, or a
+                                  reused plan made for other sizes          */
 
 /* Flags. */
 #define FM_FLAG_FORCE_INT64 0x1u /* use the 64-bit index specialisation */
+#define FM_FLAG_REUSE_PLAN 0x2u  /* attention forward: use the work order already
+                                    in the workspace (see fm_attn_fwd_plan) */
 
 /*
  * fm_rope_qk_varlen -- rotary position embedding of q and k, in place, with
@@ -212,7 +215,11 @@ FM_API size_t fm_attn_fwd_workspace_size(int64_t total_tokens, int n_seqs, int n
  *                     256-byte aligned; its contents need no initialisation
  *                     and are overwritten.  Calls that share a workspace must
  *                     be ordered on one stream.
- *   flags             FM_FLAG_FORCE_INT64 or 0.
+ *   flags             FM_FLAG_FORCE_INT64, FM_FLAG_REUSE_PLAN, both or 0.
+ *                     Without FM_FLAG_REUSE_PLAN the call first runs the
+ *                     scheduler (fm_attn_fwd_plan) into `workspace`; with it
+ *                     the call launches the attention kernel alone, on the
+ *                     work order already there (see fm_attn_fwd_plan).
  */
 FM_API fm_status fm_attn_fwd_varlen(const void* q, const void* k, const void* v, int64_t total_tokens,
                              int n_heads_q, int n_heads_kv, int head_dim,
@@ -222,6 +229,37 @@ FM_API fm_status fm_attn_fwd_varlen(const void* q, const void* k, const void* v,
                              int block_m, int block_n, void* out, float* lse,
                              int64_t* block_class_counts, void* workspace,
                              size_t workspace_bytes, uint32_t flags, void* stream);
+
+/*
+ * fm_attn_fwd_plan -- the scheduler of fm_attn_fwd_varlen alone: the work
+ * items (the real Q tiles of every sample, times Hq) and their order, largest
+ * first by the number of blocks that are not fully masked, written into
+ * `workspace` together with the sizes they were made for.
+ *
+ * Varlen-Packing technical document, section 2: a fixed grid over
+ * ceil(max_seq_len / block_m) tiles per sample leaves most of its blocks
+ * empty on packed batches; this work list holds real tiles only.  The list
+ * depends on cu_seqlens and the sizes, not on q, k or v, so the layers of a
+ * model that share one packed batch can share one plan: plan once, then pass
+ * FM_FLAG_REUSE_PLAN to every fm_attn_fwd_varlen / fm_attn_fwd_varlen_rope
+ * call on this workspace (the calls need not repeat the scheduler's two
+ * launches).  A call with the flag checks on the device that the plan was
+ * made for the same total_tokens, n_seqs, n_heads_q, block_m and block_n;
+ * if not (or once fm_attn_bwd_varlen has used the workspace, or a call on
+ * the plan has set a device error) it computes nothing and sets
+ * FM_DEVERR_DATA.  It cannot check cu_seqlens itself: the plan must come
+ * from the same cu_seqlens values.  The mask statistics only set the order
+ * (the attention kernel classifies every block itself), so a plan stays
+ * correct for other masks over the same samples.
+ *
+ * Arguments as fm_attn_fwd_varlen (same meaning and rules).  The device
+ * error word and timeout record of `workspace` are cleared.
+ */
+FM_API fm_status fm_attn_fwd_plan(int64_t total_tokens, int n_heads_q, const int32_t* cu_seqlens,
+                                  int n_seqs, const int32_t* startend_row_indices,
+                                  int n_mask_heads, const int32_t* block_minmax, int causal,
+                                  int block_m, int block_n, void* workspace,
+                                  size_t workspace_bytes, void* stream);
 
 /*
  * fm_attn_fwd_varlen_noalloc -- fm_attn_fwd_varlen for callers that cannot
@@ -243,7 +281,8 @@ FM_API fm_status fm_attn_fwd_varlen(const void* q, const void* k, const void* v,
  * overlap on the GPU race on it, so order them on one stream.  Nothing is
  * allocated or freed.  The device error word and the timeout record of the
  * last call on the current device are read with fm_get_device_error /
- * fm_get_device_timeout_info given workspace == NULL.
+ * fm_get_device_timeout_info given workspace == NULL.  Every call runs the
+ * scheduler: FM_FLAG_REUSE_PLAN gives FM_ERR_INVALID_ARG.
  */
 FM_API fm_status fm_attn_fwd_varlen_noalloc(const void* q, const void* k, const void* v,
                                             int64_t total_tokens, int n_heads_q, int n_heads_kv,

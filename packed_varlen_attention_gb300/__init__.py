@@ -12,6 +12,8 @@ Entry points (same names as the C ABI in ``include/fm.h``):
 * ``mask_block_minmax``    FlashMask per-key-tile min/max of LTS/LTE/UTS/UTE
 * ``attn_fwd_varlen``      FlashMask attention forward (out, lse)
 * ``attn_fwd_varlen_rope``  the same with the QK RoPE fused into its prologue
+* ``attn_fwd_plan``        the forward's scheduler alone (a plan that the layers
+                           of one packed batch reuse with ``reuse_plan=True``)
 * ``attn_bwd_varlen``      FlashMask attention backward (dq, dk, dv)
 """
 
@@ -37,6 +39,7 @@ __all__ = [
     "attn_fwd_num_work_items",
     "attn_bwd_workspace_size",
     "attn_bwd_varlen",
+    "attn_fwd_plan",
     "get_device_error",
     "get_device_timeout_info",
     "debug_bounded_wait",
@@ -51,6 +54,7 @@ _LIB_PATH = os.path.join(_HERE, "libfm.so")
 _LIB = None
 
 FM_FLAG_FORCE_INT64 = 0x1
+FM_FLAG_REUSE_PLAN = 0x2
 FM_DEVERR_TIMEOUT = 0x1
 FM_DEVERR_DATA = 0x2
 
@@ -72,6 +76,8 @@ _SIGNATURES = {
                                     _c_int, _c_vp, _c_int, _c_vp, _c_int, ctypes.c_float, _c_int,
                                     _c_int, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_u32,
                                     _c_vp]),
+    "fm_attn_fwd_plan": (_c_int, [_c_i64, _c_int, _c_vp, _c_int, _c_vp, _c_int, _c_vp, _c_int,
+                                  _c_int, _c_int, _c_vp, ctypes.c_size_t, _c_vp]),
     "fm_attn_fwd_varlen_noalloc": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_int, _c_int, _c_int,
                                             _c_vp, _c_int, _c_vp, _c_int, _c_vp, _c_int,
                                             ctypes.c_float, _c_int, _c_int, _c_vp, _c_vp, _c_vp,
@@ -141,6 +147,10 @@ def _stream(stream) -> int:
 
 def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else t.data_ptr()
+
+
+def _flags(force_int64: bool, reuse_plan: bool = False) -> int:
+    return (FM_FLAG_FORCE_INT64 if force_int64 else 0) | (FM_FLAG_REUSE_PLAN if reuse_plan else 0)
 
 
 def _need(t: torch.Tensor, name: str, dtype: torch.dtype):
@@ -221,8 +231,16 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
                     out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                     class_counts: Optional[torch.Tensor] = None,
                     workspace: Optional[torch.Tensor] = None, force_int64: bool = False,
+                    reuse_plan: bool = False,
                     stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """FlashMask attention forward. Returns (out [T, Hq, D] bf16, lse [Hq, T] fp32)."""
+    """FlashMask attention forward. Returns (out [T, Hq, D] bf16, lse [Hq, T] fp32).
+
+    ``reuse_plan``: launch the attention kernel alone, on the work order that
+    ``attn_fwd_plan`` (or an earlier call without the flag) left in
+    ``workspace`` for the same ``cu_seqlens`` and sizes.
+    """
+    if reuse_plan and workspace is None:
+        raise ValueError("reuse_plan needs the workspace that holds the plan")
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.bfloat16)
         if not t.is_contiguous():
@@ -251,9 +269,36 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
         _ptr(q), _ptr(k), _ptr(v), T, hq, hkv, d, _ptr(cu_seqlens), n_seqs,
         _ptr(startend_row_indices), hm, _ptr(block_minmax), int(bool(causal)),
         float(softmax_scale), block_m, block_n, _ptr(out), _ptr(lse), _ptr(class_counts),
-        _ptr(workspace), workspace.numel(), FM_FLAG_FORCE_INT64 if force_int64 else 0,
+        _ptr(workspace), workspace.numel(), _flags(force_int64, reuse_plan),
         _stream(stream)))
     return out, lse
+
+
+def attn_fwd_plan(cu_seqlens: torch.Tensor, total_tokens: int, n_heads_q: int,
+                  startend_row_indices: Optional[torch.Tensor] = None,
+                  block_minmax: Optional[torch.Tensor] = None, causal: bool = False,
+                  block_m: int = 128, block_n: int = 128,
+                  workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The forward scheduler alone: writes the work order for these samples
+    into ``workspace`` (allocated when None) and returns it, for attention
+    calls given ``reuse_plan=True``."""
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    n_seqs = cu_seqlens.numel() - 1
+    hm = 0
+    if startend_row_indices is not None:
+        _need(startend_row_indices, "startend_row_indices", torch.int32)
+        hm = startend_row_indices.shape[0]
+        if block_minmax is None:
+            raise ValueError("block_minmax (from mask_block_minmax) is required with a mask")
+        _need(block_minmax, "block_minmax", torch.int32)
+    if workspace is None:
+        nbytes = attn_fwd_workspace_size(total_tokens, n_seqs, n_heads_q, block_m)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=cu_seqlens.device)
+    _check("fm_attn_fwd_plan", _lib().fm_attn_fwd_plan(
+        total_tokens, n_heads_q, _ptr(cu_seqlens), n_seqs, _ptr(startend_row_indices), hm,
+        _ptr(block_minmax), int(bool(causal)), block_m, block_n, _ptr(workspace),
+        workspace.numel(), _stream(stream)))
+    return workspace
 
 
 def attn_fwd_varlen_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
@@ -310,6 +355,7 @@ def attn_fwd_varlen_rope(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                          q_rot: Optional[torch.Tensor] = None,
                          class_counts: Optional[torch.Tensor] = None,
                          workspace: Optional[torch.Tensor] = None, force_int64: bool = False,
+                         reuse_plan: bool = False,
                          stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Attention forward with the QK RoPE fused into its prologue.
 
@@ -317,8 +363,10 @@ def attn_fwd_varlen_rope(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     ``q`` is rotated tile by tile in shared memory and left unchanged, unless
     ``q_rot`` (written with the rotated queries) is ``q`` itself.  Returns
     (out, lse), bit-identical to ``rope_qk_varlen`` followed by
-    ``attn_fwd_varlen``.
+    ``attn_fwd_varlen``.  ``reuse_plan`` as in ``attn_fwd_varlen``.
     """
+    if reuse_plan and workspace is None:
+        raise ValueError("reuse_plan needs the workspace that holds the plan")
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.bfloat16)
         if not t.is_contiguous():
@@ -351,7 +399,7 @@ def attn_fwd_varlen_rope(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
         float(theta), _ptr(startend_row_indices), hm, _ptr(block_minmax), int(bool(causal)),
         float(softmax_scale), block_m, block_n, _ptr(out), _ptr(lse), _ptr(q_rot),
         _ptr(class_counts), _ptr(workspace), workspace.numel(),
-        FM_FLAG_FORCE_INT64 if force_int64 else 0, _stream(stream)))
+        _flags(force_int64, reuse_plan), _stream(stream)))
     return out, lse
 
 

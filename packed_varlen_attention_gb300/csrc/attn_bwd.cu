@@ -454,6 +454,9 @@ __global__ void __launch_bounds__(kCostBins) bwd_plan_order_kernel(const AttnBwd
 #pragma unroll
       for (int i = 0; i < 4; ++i) p.ws->diag[i] = 0;
     }
+    // the tables after the header now hold the backward's order: a forward
+    // plan in this workspace is gone
+    p.ws->plan_n_seqs = 0;
   }
   __syncthreads();
   if (Mode == kModeDKV && by_steps) {

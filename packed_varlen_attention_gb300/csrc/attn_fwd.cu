@@ -373,6 +373,12 @@ __global__ void __launch_bounds__(kCostBins) plan_order_kernel(const AttnParams 
     hd->error_word = bad ? static_cast<int>(FM_DEVERR_DATA) : 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) hd->diag[i] = 0;
+    hd->exit_counter = 0u;
+    hd->plan_T = static_cast<int32_t>(p.T);
+    hd->plan_n_seqs = p.n_seqs;
+    hd->plan_hq = p.hq;
+    hd->plan_block_m = p.block_m;
+    hd->plan_block_n = p.block_n;
   }
 }
 
@@ -498,7 +504,23 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
 
   if (warp == 0) {
     // --------------------------------------------------- K producer + metadata
-    const int n_items = p.ws->n_items;
+    int n_items = 0;
+    {
+      // A plan made for other sizes (or overwritten since) is not used; a
+      // reused plan is not used either once a call on it has set an error
+      // (its counters may not have been reset).  Either way no item runs.
+      const AttnWorkspaceHeader* hd = p.ws;
+      const bool fits = hd->plan_n_seqs == p.n_seqs && hd->plan_T == static_cast<int32_t>(p.T) &&
+                        hd->plan_hq == p.hq && hd->plan_block_m == p.block_m &&
+                        hd->plan_block_n == p.block_n;
+      if (!fits) {
+        if (lane == 0) atomicOr(&p.ws->error_word, static_cast<int>(FM_DEVERR_DATA));
+      } else if (!(p.reuse_plan && hd->error_word != 0)) {
+        const int64_t cap = p.n_qslots * p.hq;  // entries the order table can hold
+        n_items = static_cast<int>(max(static_cast<int64_t>(0),
+                                       min(static_cast<int64_t>(hd->n_items), cap)));
+      }
+    }
     const int group = p.hq / p.hkv;
     constexpr uint32_t NKV = kKVSlots<BN>, NQ = kQSlots<BN>;
     uint32_t kv_t = 0;               // KV tiles loaded (K(t) is ring load 2t)
@@ -608,18 +630,30 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       if (lane == 0) item = static_cast<int>(atomicAdd(&p.ws->work_counter, 1u));
       item = __shfl_sync(0xffffffffu, item, 0);
       if (item >= n_items) {
+        if (lane == 0) {
+          // every CTA claims past the end exactly once; the last one to do
+          // so resets the counters, so that the plan can be used again
+          __threadfence();
+          if (atomicAdd(&p.ws->exit_counter, 1u) == gridDim.x - 1u) {
+            p.ws->work_counter = 0u;
+            p.ws->exit_counter = 0u;
+          }
+        }
         ok = push_meta(kStop, kClsF, kClsF, 0, 0, 0, 0, 0, 0, false, 0, 0, 0u);
         break;
       }
       const int2 pi = p.order[item / p.hq];
       const int h = item % p.hq;
-      const int s = pi.x;
+      // an entry the planner never writes becomes an empty item (no rows)
+      const bool bad_entry = pi.x < 0 || pi.x >= p.n_seqs || pi.y < 0;
+      if (bad_entry && lane == 0) atomicOr(&p.ws->error_word, static_cast<int>(FM_DEVERR_DATA));
+      const int s = bad_entry ? 0 : pi.x;
       const int kvh = h / group;
       const int mh = p.hm > 1 ? h : 0;
       const int a = clamp_tok(__ldg(p.cu + s), T);
       const int b = max(a, clamp_tok(__ldg(p.cu + s + 1), T));
       int r0, r1, r2;
-      item_rows<QT>(a, b, pi.y, BM, r0, r1, r2);
+      item_rows<QT>(a, b, bad_entry ? (1 << 30) : pi.y, BM, r0, r1, r2);
       const bool has_q1 = r2 > r1;  // (never with one Q tile per item)
       const int n_kv = (b - a + BN - 1) / BN;
       const int kt_end = (r2 > r0) ? kv_tiles_to_scan<BN>(p, a, b, r2) : 0;
@@ -1572,6 +1606,15 @@ __global__ void bounded_wait_probe_kernel(int32_t* status, uint64_t timeout_ns) 
   if (threadIdx.x == 0) *status = ok ? FM_OK : FM_ERR_TIMEOUT;
 }
 
+template <int BN, int QT>
+cudaError_t launch_plan(const AttnParams& p, cudaStream_t stream) {
+  cudaError_t e = launch_pdl(plan_cost_kernel<BN, QT>,
+                             dim3(static_cast<unsigned>((p.n_qslots + 7) / 8)), dim3(256), 0,
+                             stream, p);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(plan_order_kernel, dim3(1), dim3(kCostBins), 0, stream, p);
+}
+
 template <int D, int BN, int QT, typename IdxT, bool ROPE>
 cudaError_t launch_typed(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const RopeArgs& ra, int num_sms,
@@ -1595,11 +1638,10 @@ cudaError_t launch_typed(const AttnParams& p, const CUtensorMap& tq, const CUten
     if (dev < 64) configured |= 1ull << dev;
   }
   const int64_t n_slots = p.n_qslots;
-  e = launch_pdl(plan_cost_kernel<BN, QT>, dim3(static_cast<unsigned>((n_slots + 7) / 8)),
-                 dim3(256), 0, stream, p);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(plan_order_kernel, dim3(1), dim3(kCostBins), 0, stream, p);
-  if (e != cudaSuccess) return e;
+  if (!p.reuse_plan) {
+    e = launch_plan<BN, QT>(p, stream);
+    if (e != cudaSuccess) return e;
+  }
   const int64_t max_items = n_slots * p.hq;
   const int grid = static_cast<int>(max_items < num_sms ? max_items : num_sms);
   return launch_pdl(attn_fwd_kernel<D, BN, QT, IdxT, ROPE>, dim3(grid), dim3(kThreads<QT>),
@@ -1647,6 +1689,11 @@ cudaError_t launch_attn_fwd(const AttnParams& p, const CUtensorMap& tq, const CU
   RopeArgs none;
   memset(&none, 0, sizeof(none));
   return launch_attn_dispatch<false>(p, tq, tk, tv, none, use_int64, num_sms, stream);
+}
+
+cudaError_t launch_attn_plan(const AttnParams& p, cudaStream_t stream) {
+  return p.block_n == 128 ? launch_plan<128, kQTilesBN128>(p, stream)
+                          : launch_plan<64, 2>(p, stream);
 }
 
 cudaError_t launch_bounded_wait_probe(int32_t* status, uint64_t timeout_ns, cudaStream_t stream) {

@@ -72,6 +72,8 @@ extern "C" fm_status fm_attn_fwd_varlen_noalloc(
     const int32_t* startend_row_indices, int n_mask_heads, const int32_t* block_minmax,
     int causal, float softmax_scale, int block_m, int block_n, void* out, float* lse,
     int64_t* block_class_counts, uint32_t flags, void* stream) {
+  // the shared array holds whichever call ran last: no plan is reused here
+  if (flags & FM_FLAG_REUSE_PLAN) return FM_ERR_INVALID_ARG;
   if (total_tokens < 0 || n_seqs < 1 || (block_m != 64 && block_m != 128))
     return total_tokens < 0 || n_seqs < 1 ? FM_ERR_INVALID_ARG : FM_ERR_UNSUPPORTED;
   if (total_tokens / block_m + n_seqs > kMaxQSlots) return FM_ERR_WORKSPACE;

@@ -204,6 +204,62 @@ void rope_freqs(double theta, int head_dim, fm::RopeFreqs* fr) {
   }
 }
 
+// The scheduler's part of the forward parameters: samples, mask statistics,
+// tile sizes and the workspace tables (shared by the attention calls and
+// fm_attn_fwd_plan, so that a plan and the calls that reuse it agree).
+void set_schedule_params(AttnParams& p, int64_t total_tokens, int n_heads_q,
+                         const int32_t* cu_seqlens, int n_seqs,
+                         const int32_t* startend_row_indices, int n_mask_heads,
+                         const int32_t* block_minmax, int causal, int block_m, int block_n,
+                         void* workspace) {
+  const int64_t n_qslots = total_tokens / block_m + n_seqs;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.cu = cu_seqlens;
+  p.sri = startend_row_indices;
+  p.minmax = block_minmax;
+  p.ws = reinterpret_cast<fm::AttnWorkspaceHeader*>(ws);
+  uint8_t* tail = ws + sizeof(fm::AttnWorkspaceHeader);
+  p.slot_info = reinterpret_cast<int2*>(tail);
+  p.order = reinterpret_cast<int2*>(tail + n_qslots * sizeof(int2));
+  p.cost = reinterpret_cast<int*>(tail + 2 * n_qslots * sizeof(int2));
+  p.T = total_tokens;
+  p.n_qslots = n_qslots;
+  p.n_kv_slots = fm_num_kv_tiles_bound(total_tokens, n_seqs, block_n);
+  p.n_seqs = n_seqs;
+  p.hq = n_heads_q;
+  p.hm = n_mask_heads;
+  p.block_m = block_m;
+  p.block_n = block_n;
+  p.causal = causal != 0;
+}
+
+// Validation shared by the attention forward calls and fm_attn_fwd_plan:
+// samples, mask arguments (n_mask_heads is set to 0 without a mask), tile
+// sizes and workspace.
+fm_status check_schedule_args(int64_t total_tokens, int n_heads_q, const int32_t* cu_seqlens,
+                              int n_seqs, const int32_t* startend_row_indices,
+                              int& n_mask_heads, const int32_t* block_minmax, int block_m,
+                              int block_n, const void* workspace, size_t workspace_bytes) {
+  if (cu_seqlens == nullptr || workspace == nullptr) return FM_ERR_INVALID_ARG;
+  if (total_tokens < 0 || total_tokens > INT32_MAX - 256 || n_seqs < 1) return FM_ERR_INVALID_ARG;
+  if (n_heads_q < 1) return FM_ERR_INVALID_ARG;
+  if (startend_row_indices != nullptr) {
+    if (n_mask_heads != 1 && n_mask_heads != n_heads_q) return FM_ERR_INVALID_ARG;
+    if (block_minmax == nullptr) return FM_ERR_INVALID_ARG;
+  } else {
+    if (block_minmax != nullptr) return FM_ERR_INVALID_ARG;
+    n_mask_heads = 0;
+  }
+  if ((block_m != 64 && block_m != 128) || (block_n != 64 && block_n != 128))
+    return FM_ERR_UNSUPPORTED;
+  if (!aligned(workspace, 256)) return FM_ERR_ALIGNMENT;
+  if (workspace_bytes < fm::attn_workspace_bytes(total_tokens, n_seqs, block_m))
+    return FM_ERR_WORKSPACE;
+  const int64_t n_qslots = total_tokens / block_m + n_seqs;
+  if (n_qslots * n_heads_q >= (int64_t(1) << 31)) return FM_ERR_UNSUPPORTED;
+  return FM_OK;
+}
+
 // fm_attn_fwd_varlen and fm_attn_fwd_varlen_rope: validation, tensor maps,
 // parameters and launches.  With `theta` > 0 the keys are rotated in place
 // first and every Q tile is rotated in shared memory after its load.
@@ -220,34 +276,23 @@ fm_status attn_fwd_impl(const void* q, void* k_rot_in_place, const void* k, cons
   if (fused_rope && (k_rot_in_place == nullptr || k_rot_in_place != k)) return FM_ERR_INVALID_ARG;
   if (!fused_rope && q_rot != nullptr) return FM_ERR_INVALID_ARG;
   if (q_rot != nullptr && !aligned(q_rot, 16)) return FM_ERR_ALIGNMENT;
-  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || lse == nullptr ||
-      cu_seqlens == nullptr || workspace == nullptr)
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || lse == nullptr)
     return FM_ERR_INVALID_ARG;
-  if (total_tokens < 0 || total_tokens > INT32_MAX - 256 || n_seqs < 1) return FM_ERR_INVALID_ARG;
-  if (n_heads_q < 1 || n_heads_kv < 1 || n_heads_q % n_heads_kv != 0) return FM_ERR_INVALID_ARG;
-  if (flags & ~FM_FLAG_FORCE_INT64) return FM_ERR_INVALID_ARG;
-  if (startend_row_indices != nullptr) {
-    if (n_mask_heads != 1 && n_mask_heads != n_heads_q) return FM_ERR_INVALID_ARG;
-    if (block_minmax == nullptr) return FM_ERR_INVALID_ARG;
-  } else {
-    if (block_minmax != nullptr) return FM_ERR_INVALID_ARG;
-    n_mask_heads = 0;
-  }
+  if (n_heads_kv < 1 || n_heads_q < 1 || n_heads_q % n_heads_kv != 0) return FM_ERR_INVALID_ARG;
+  if (flags & ~(FM_FLAG_FORCE_INT64 | FM_FLAG_REUSE_PLAN)) return FM_ERR_INVALID_ARG;
+  fm_status st = check_schedule_args(total_tokens, n_heads_q, cu_seqlens, n_seqs,
+                                     startend_row_indices, n_mask_heads, block_minmax, block_m,
+                                     block_n, workspace, workspace_bytes);
+  if (st != FM_OK) return st;
   if (!(softmax_scale >= 0.0f) || !std::isfinite(softmax_scale)) return FM_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return FM_ERR_UNSUPPORTED;
-  if ((block_m != 64 && block_m != 128) || (block_n != 64 && block_n != 128))
-    return FM_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
-      !aligned(lse, 4) || !aligned(workspace, 256))
+      !aligned(lse, 4))
     return FM_ERR_ALIGNMENT;
   if (block_class_counts != nullptr && !aligned(block_class_counts, 8)) return FM_ERR_ALIGNMENT;
-  if (workspace_bytes < fm::attn_workspace_bytes(total_tokens, n_seqs, block_m))
-    return FM_ERR_WORKSPACE;
-  const int64_t n_qslots = total_tokens / block_m + n_seqs;
-  if (n_qslots * n_heads_q >= (int64_t(1) << 31)) return FM_ERR_UNSUPPORTED;
   if (total_tokens == 0) return FM_OK;
   int num_sms = 0;
-  fm_status st = device_info(&num_sms);
+  st = device_info(&num_sms);
   if (st != FM_OK) return st;
 
   CUtensorMap tq, tk, tv;
@@ -259,32 +304,17 @@ fm_status attn_fwd_impl(const void* q, void* k_rot_in_place, const void* k, cons
 
   AttnParams p;
   std::memset(&p, 0, sizeof(p));
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  set_schedule_params(p, total_tokens, n_heads_q, cu_seqlens, n_seqs, startend_row_indices,
+                      n_mask_heads, block_minmax, causal, block_m, block_n, workspace);
   p.q = q;
   p.k = k;
   p.v = v;
   p.out = out;
   p.lse = lse;
-  p.cu = cu_seqlens;
-  p.sri = startend_row_indices;
-  p.minmax = block_minmax;
   p.class_counts = block_class_counts;
-  p.ws = reinterpret_cast<fm::AttnWorkspaceHeader*>(ws);
-  uint8_t* tail = ws + sizeof(fm::AttnWorkspaceHeader);
-  p.slot_info = reinterpret_cast<int2*>(tail);
-  p.order = reinterpret_cast<int2*>(tail + n_qslots * sizeof(int2));
-  p.cost = reinterpret_cast<int*>(tail + 2 * n_qslots * sizeof(int2));
-  p.T = total_tokens;
-  p.n_qslots = n_qslots;
-  p.n_kv_slots = fm_num_kv_tiles_bound(total_tokens, n_seqs, block_n);
-  p.n_seqs = n_seqs;
-  p.hq = n_heads_q;
   p.hkv = n_heads_kv;
-  p.hm = n_mask_heads;
   p.head_dim = head_dim;
-  p.block_m = block_m;
-  p.block_n = block_n;
-  p.causal = causal != 0;
+  p.reuse_plan = (flags & FM_FLAG_REUSE_PLAN) != 0;
   const double scale = softmax_scale > 0.0f ? softmax_scale : 1.0 / std::sqrt(double(head_dim));
   p.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
   p.timeout_ns = 1000000000ull;
@@ -293,7 +323,8 @@ fm_status attn_fwd_impl(const void* q, void* k_rot_in_place, const void* k, cons
   const bool use64 =
       fm_attn_index_bits(total_tokens, n_heads_q, n_heads_kv, head_dim, flags) == 64;
 
-  // (the planner initialises the workspace header itself: no memset)
+  // (the planner initialises the workspace header itself: no memset; with
+  // FM_FLAG_REUSE_PLAN the kernel checks the stored plan's sizes instead)
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (!fused_rope) return from_cuda(fm::launch_attn_fwd(p, tq, tk, tv, use64, num_sms, s));
 
@@ -341,6 +372,25 @@ fm_status fm_attn_fwd_varlen_rope(const void* q, void* k, const void* v, int64_t
                        n_seqs, startend_row_indices, n_mask_heads, block_minmax, causal,
                        softmax_scale, block_m, block_n, theta, out, lse, q_rot,
                        block_class_counts, workspace, workspace_bytes, flags, stream);
+}
+
+fm_status fm_attn_fwd_plan(int64_t total_tokens, int n_heads_q, const int32_t* cu_seqlens,
+                           int n_seqs, const int32_t* startend_row_indices, int n_mask_heads,
+                           const int32_t* block_minmax, int causal, int block_m, int block_n,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  fm_status st = check_schedule_args(total_tokens, n_heads_q, cu_seqlens, n_seqs,
+                                     startend_row_indices, n_mask_heads, block_minmax, block_m,
+                                     block_n, workspace, workspace_bytes);
+  if (st != FM_OK) return st;
+  if (total_tokens == 0) return FM_OK;
+  int num_sms = 0;
+  st = device_info(&num_sms);
+  if (st != FM_OK) return st;
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  set_schedule_params(p, total_tokens, n_heads_q, cu_seqlens, n_seqs, startend_row_indices,
+                      n_mask_heads, block_minmax, causal, block_m, block_n, workspace);
+  return from_cuda(fm::launch_attn_plan(p, static_cast<cudaStream_t>(stream)));
 }
 
 size_t fm_attn_bwd_workspace_size(int64_t total_tokens, int n_seqs, int n_heads_q) {

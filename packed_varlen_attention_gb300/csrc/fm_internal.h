@@ -69,7 +69,10 @@ struct AttnWorkspaceHeader {
   uint32_t work_counter_kv;  // backward: next key/value work item (atomic)
   int32_t bwd_q_tiles;       // backward: real 128-row tiles (planner)
   int32_t bwd_kv_tiles;      // backward: the same count for the key/value pass
-  int32_t pad[52];
+  // forward plan: the sizes it was made for (plan_n_seqs = 0: no valid plan)
+  int32_t plan_T, plan_n_seqs, plan_hq, plan_block_m, plan_block_n;
+  uint32_t exit_counter;  // forward: CTAs done claiming (the last one resets the counters)
+  int32_t pad[46];
 };
 static_assert(sizeof(AttnWorkspaceHeader) == 256, "header is 256 bytes");
 
@@ -97,6 +100,7 @@ struct AttnParams {
   int head_dim;
   int block_m, block_n;
   int causal;
+  int reuse_plan;  // skip the planner: the workspace holds the work order already
   float scale_log2;
   uint64_t timeout_ns;
 };
@@ -112,6 +116,9 @@ void* noalloc_scratch_address(fm_status* st);
 cudaError_t launch_attn_fwd(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, bool use_int64, int num_sms,
                             cudaStream_t stream, const RopeArgs* rope = nullptr);
+
+// The forward scheduler alone (the planner kernels of launch_attn_fwd).
+cudaError_t launch_attn_plan(const AttnParams& p, cudaStream_t stream);
 
 cudaError_t launch_bounded_wait_probe(int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 

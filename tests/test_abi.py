@@ -111,6 +111,27 @@ def test_validation_rejects_before_any_launch(fm):
     assert attn_rope(k=None) == 1
     assert attn_rope(q_rot=ctypes.c_void_p(0x10008)) == 3
     assert attn_rope(hq=3) == 1
+    # the scheduler alone: the same sample, mask, tile and workspace rules
+    def plan(cu=fake, hq=4, sri=None, hm=0, mm=None, bm=128, bn=128, ws=fake, ws_bytes=1 << 20,
+             T=256):
+        return lib.fm_attn_fwd_plan(T, hq, cu, 2, sri, hm, mm, 1, bm, bn, ws, ws_bytes, None)
+    assert plan(cu=None) == 1
+    assert plan(ws=None) == 1
+    assert plan(T=-1) == 1
+    assert plan(hq=0) == 1
+    assert plan(sri=fake, hm=3, mm=fake) == 1
+    assert plan(sri=fake, hm=1, mm=None) == 1
+    assert plan(bm=96) == 2
+    assert plan(bn=32) == 2
+    assert plan(ws=ctypes.c_void_p(0x10010)) == 3
+    assert plan(ws_bytes=16) == 4
+    assert plan(T=0) == 0  # nothing to schedule: no launch
+    # flags: unknown bits are refused; the allocation-free call never reuses a plan
+    assert lib.fm_attn_fwd_varlen(fake, fake, fake, 256, 4, 2, 128, fake, 2, None, 0, None, 1,
+                                  0.0, 128, 128, fake, fake, None, fake, 1 << 20, 4, None) == 1
+    assert lib.fm_attn_fwd_varlen_noalloc(fake, fake, fake, 256, 4, 2, 128, fake, 2, None, 0, None,
+                                          1, 0.0, 128, 128, fake, fake, None,
+                                          fm.FM_FLAG_REUSE_PLAN, None) == 1
     assert lib.fm_debug_bounded_wait(fake, 0, None) == 1
 
 
