@@ -377,8 +377,7 @@ __global__ void __launch_bounds__(kCostBins) plan_order_kernel(const AttnParams 
     hd->plan_T = static_cast<int32_t>(p.T);
     hd->plan_n_seqs = p.n_seqs;
     hd->plan_hq = p.hq;
-    hd->plan_block_m = p.block_m;
-    hd->plan_block_n = p.block_n;
+    hd->plan_tiles = p.block_m | (p.block_n << 16);
   }
 }
 
@@ -509,16 +508,18 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       // A plan made for other sizes (or overwritten since) is not used; a
       // reused plan is not used either once a call on it has set an error
       // (its counters may not have been reset).  Either way no item runs.
-      const AttnWorkspaceHeader* hd = p.ws;
-      const bool fits = hd->plan_n_seqs == p.n_seqs && hd->plan_T == static_cast<int32_t>(p.T) &&
-                        hd->plan_hq == p.hq && hd->plan_block_m == p.block_m &&
-                        hd->plan_block_n == p.block_n;
+      // two independent 16-byte loads: {work counter, Q tiles, items, error
+      // word} and the plan's sizes
+      const int4 h0 = *reinterpret_cast<const int4*>(p.ws);
+      const int4 hp = *reinterpret_cast<const int4*>(&p.ws->plan_T);
+      const bool fits = (hp.x == static_cast<int32_t>(p.T)) & (hp.y == p.n_seqs) &
+                        (hp.z == p.hq) & (hp.w == (p.block_m | (p.block_n << 16)));
       if (!fits) {
         if (lane == 0) atomicOr(&p.ws->error_word, static_cast<int>(FM_DEVERR_DATA));
-      } else if (!(p.reuse_plan && hd->error_word != 0)) {
+      } else if (!(p.reuse_plan && h0.w != 0)) {
         const int64_t cap = p.n_qslots * p.hq;  // entries the order table can hold
         n_items = static_cast<int>(max(static_cast<int64_t>(0),
-                                       min(static_cast<int64_t>(hd->n_items), cap)));
+                                       min(static_cast<int64_t>(h0.z), cap)));
       }
     }
     const int group = p.hq / p.hkv;

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include <utility>
@@ -69,12 +70,17 @@ struct AttnWorkspaceHeader {
   uint32_t work_counter_kv;  // backward: next key/value work item (atomic)
   int32_t bwd_q_tiles;       // backward: real 128-row tiles (planner)
   int32_t bwd_kv_tiles;      // backward: the same count for the key/value pass
-  // forward plan: the sizes it was made for (plan_n_seqs = 0: no valid plan)
-  int32_t plan_T, plan_n_seqs, plan_hq, plan_block_m, plan_block_n;
+  // forward plan: the sizes it was made for (plan_n_seqs = 0: no valid plan),
+  // one 16-byte group read with one load; plan_tiles = block_m | block_n << 16
+  int32_t plan_T, plan_n_seqs, plan_hq, plan_tiles;
   uint32_t exit_counter;  // forward: CTAs done claiming (the last one resets the counters)
-  int32_t pad[46];
+  int32_t pad[47];
 };
 static_assert(sizeof(AttnWorkspaceHeader) == 256, "header is 256 bytes");
+static_assert(offsetof(AttnWorkspaceHeader, n_items) == 8 &&
+                  offsetof(AttnWorkspaceHeader, error_word) == 12 &&
+                  offsetof(AttnWorkspaceHeader, plan_T) % 16 == 0,
+              "the attention kernel reads the header in 16-byte groups");
 
 constexpr int kCostBins = 1024;  // scheduler histogram bins (cost = non-F KV tiles)
 
