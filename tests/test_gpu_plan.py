@@ -84,6 +84,28 @@ def test_reused_plan_gives_the_bits_of_a_fresh_call(fm, cfg):
                     wl=wl)
 
 
+@pytest.mark.parametrize("head_dim,block", [(64, 64), (128, 64), (64, 128)])
+def test_reused_plan_other_tile_shapes(fm, head_dim, block):
+    """The 64-row / 64-column tile kernels and head_dim 64 on one plan, two
+    layers: the bits of calls that plan for themselves, and the oracle."""
+    import torch
+    from test_gpu_attn import oracle
+    wl = gen.make_custom([300, 77, 1000, 129, 64], n_heads_q=4, n_heads_kv=2,
+                         head_dim=head_dim, block_m=block, block_n=block,
+                         mask="causal_document", seed=17)
+    b = Batch(fm, wl, n_layers=2)
+    ws = b.plan(fm)
+    for layer in range(2):
+        out_r, lse_r = b.attn(fm, layer, ws, True)
+        out_f, lse_f = b.attn(fm, layer, None, False)
+        torch.cuda.synchronize()
+        assert fm.get_device_error(ws) == 0
+        assert _same(out_r, out_f) and _same(lse_r, lse_f), f"layer {layer}"
+        if layer == 0:
+            compare(out_r, lse_r, oracle(wl), what=f"D={head_dim} block {block} reused plan",
+                    wl=wl)
+
+
 def test_reused_plan_with_fused_rope(fm):
     import torch
     wl = gen.make_workload(2, seed=1)
