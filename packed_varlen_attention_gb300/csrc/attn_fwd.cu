@@ -9,26 +9,34 @@
 // the backward operator consumes (section 3.4).
 //
 // How it runs on GB300:
-//   * Planner (two tiny kernels): one warp per sample-local pair of Q tiles
-//     counts the blocks that are not fully masked (its cost); one CTA orders
-//     the real pairs by cost, largest first (counting sort over cost bins).
+//   * Planner (two tiny kernels, also callable alone so that the layers of
+//     one packed batch share one plan): one warp per sample-local pair of Q
+//     tiles counts the blocks that are not fully masked (its cost); one CTA
+//     orders the real pairs by cost, largest first (counting sort over cost
+//     bins), and writes the header (item count, the sizes planned for).
 //     Only real tiles become work -- not the fixed grid
 //     (seq_count, n_head, ceil(max_seq_len / Br)) of the Varlen-Packing
 //     technical document, section 2, whose CTAs past a short sample's end do
-//     nothing.
-//   * Persistent main kernel, one CTA per SM, pulling items (two consecutive
-//     Q tiles of one sample x one q head) from an atomic counter.  The two Q
-//     tiles share every K/V tile the CTA loads.  Warp roles (384 threads):
-//       warp 0      K producer: classifies the item's KV tiles for both Q
-//                   tiles (warp-parallel, 32 tiles per step), publishes
-//                   per-tile metadata (and the mask columns of partially
-//                   masked tiles) in a 4-slot ring, TMA-loads both Q tiles
-//                   once per item and K per tile into a 2-stage ring;
-//       warp 2      V producer: TMA-loads V per tile into a 2-stage ring;
-//       warp 1      MMA issuer (one thread): tcgen05.mma kind::f16, bf16 in,
-//                   fp32 accumulate: S_i = Q_i K^T into TMEM (i = 0, 1), then
-//                   O_i += P_i V with P_i read from TMEM (it overwrites the
-//                   first half of S_i's columns as packed bf16);
+//     nothing.  Pairs are formed from the sample's end, so a sample with an
+//     odd number of Q tiles leaves its first (under a causal mask cheapest)
+//     tile unpaired.
+//   * Persistent main kernel, one CTA per SM, pulling items (a pair of Q
+//     tiles of one sample x one q head) from an atomic counter; the last CTA
+//     to finish claiming resets the counter, so a plan can be used again.
+//     The two Q tiles share every K/V tile the CTA loads.  Warp roles (384
+//     threads; warps 0..3 at 96 registers, the softmax warpgroups at 200):
+//       warp 0      K producer: checks the plan's sizes, classifies the
+//                   item's KV tiles for both Q tiles (warp-parallel, 32 tiles
+//                   per step), loads Q tile 0 into the Q ring right after,
+//                   then publishes per-tile metadata (and the mask columns of
+//                   partially masked tiles) in a 4-slot ring and TMA-loads K
+//                   per tile into the K/V ring (Q tile 1 after the first K);
+//       warp 2      V producer: TMA-loads V per tile into the same ring;
+//       warps 1, 3  MMA issuers, one per Q tile, taking strict turns
+//                   (tcgen05.mma kind::f16, bf16 in, fp32 accumulate): S_i =
+//                   Q_i K^T into TMEM, then O_i += P_i V with P_i read from
+//                   TMEM (it overwrites the first half of S_i's columns as
+//                   packed bf16);
 //       warps 4..7  softmax of Q tile 0, warps 8..11 softmax of Q tile 1: one
 //                   thread per tile row (= TMEM lane).  The whole S row is
 //                   loaded from TMEM with one wait, masked (partial blocks
@@ -36,7 +44,7 @@
 //                   P = 2^(S*scale*log2e - m) with a running sum and stored as
 //                   bf16 into TMEM.  O_i is rescaled in TMEM only when the max
 //                   grew by more than 2^8; the epilogue normalises O_i and
-//                   writes out / lse with guarded stores.
+//                   writes out / lse through shared-memory staging.
 //     The MMA order per KV tile is PV_0, S_0(next), PV_1, S_1(next): while one
 //     softmax warpgroup works, the tensor cores run the other tile's MMAs.
 //   * Every mbarrier wait is bounded (wall-clock limit) and reports
