@@ -528,8 +528,8 @@ def median_entry(fl, rb, attn_ms_median, rope_ms_median, peaks, n):
 
 
 def time_backward(fm, torch, batch, steps, warmup, flush):
-    """Mean device time (ms) of one fm_attn_bwd_varlen call (prep + dK/dV +
-    dQ kernels), L2 flushed before each call."""
+    """Mean device time (ms) of one fm_attn_bwd_varlen call (prep, then each
+    pass's planner and kernel), L2 flushed before each call."""
     batch.prepare_backward(fm)
     for _ in range(warmup):
         batch.backward(fm)
@@ -806,10 +806,11 @@ def run_ours(args):
                             "the write part undercounts",
         },
         "backward": dict(backward_entry(fl, bwd_ms, peaks), **{
-            "call": "attn_bwd_varlen (prep + dK/dV kernel + dQ kernel), same batch, dout seeded",
+            "call": "attn_bwd_varlen (prep, then planner + dK/dV kernel, planner + dQ kernel), "
+                    "same batch, dout seeded",
             "bound": "tensor", "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
             "peak_source": f"{peak_src} bf16 burst",
-            "launches_per_call": 3}),
+            "launches_per_call": 5}),
         "rope": {"bound": "hbm", "achieved": rope_gbs, "unit": "GB/s",
                  "peak": peaks["hbm_gbs"], "frac": rope_gbs / peaks["hbm_gbs"],
                  "frac_of_8tbs": rope_gbs / 8000.0, "bytes": rb},

@@ -15,7 +15,8 @@
 // The same block classes as the forward pass (section 3.2) skip fully masked
 // blocks and restrict the element mask to partially masked ones.
 //
-// How it runs on GB300 -- three launches, every sum owned by one CTA (no
+// How it runs on GB300 -- five launches (prep, then a one-CTA planner and
+// the persistent kernel for each pass), every sum owned by one CTA (no
 // atomics, so the gradients are bitwise reproducible):
 //   * prep: one pass over out and dout: -delta_i and -lse_i * log2(e) per
 //     (head, row) into the workspace (fp32).
