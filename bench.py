@@ -350,7 +350,8 @@ class Batch:
             events[2].record()
         split = events is not None and len(events) == 5
         if split:
-            fm.attn_fwd_plan(self.cu, wl.total_tokens, wl.n_heads_q, self.sri, self.mm,
+            fm.attn_fwd_plan(self.cu, wl.total_tokens, wl.n_heads_q, wl.n_heads_kv, self.sri,
+                             self.mm,
                              causal=wl.causal, block_m=wl.block_m, block_n=wl.block_n,
                              workspace=self.ws)
             events[3].record()

@@ -188,7 +188,11 @@ FM_API size_t fm_attn_fwd_workspace_size(int64_t total_tokens, int n_seqs, int n
  * fixed grid (seq_count, n_head, ceil(max_seq_len / block_m)) that this call
  * does not use): work items are only the real Q tiles of every sample
  * (times Hq heads), ordered by the number of blocks they must compute and
- * pulled by a persistent grid of one CTA per SM.
+ * pulled by a persistent grid of one CTA per SM.  A work item is one Q
+ * tile for two q heads that share a key/value head and the mask (when
+ * Hq / Hkv is even and n_mask_heads <= 1), else two consecutive Q tiles of
+ * one q head; either way one CTA computes both with each K/V tile loaded
+ * once.
  *
  *   q                 device bf16 [T][Hq][D], contiguous, 16-byte aligned.
  *   k, v              device bf16 [T][Hkv][D], contiguous, 16-byte aligned.
@@ -244,7 +248,8 @@ FM_API fm_status fm_attn_fwd_varlen(const void* q, const void* k, const void* v,
  * FM_FLAG_REUSE_PLAN to every fm_attn_fwd_varlen / fm_attn_fwd_varlen_rope
  * call on this workspace (the calls need not repeat the scheduler's two
  * launches).  A call with the flag checks on the device that the plan was
- * made for the same total_tokens, n_seqs, n_heads_q, block_m and block_n;
+ * made for the same total_tokens, n_seqs, n_heads_q, block_m, block_n and
+ * work-item form (see fm_attn_fwd_varlen, Scheduling);
  * if not (or once fm_attn_bwd_varlen has used the workspace, or a call on
  * the plan has set a device error) it computes nothing and sets
  * FM_DEVERR_DATA.  It cannot check cu_seqlens itself: the plan must come
@@ -255,11 +260,12 @@ FM_API fm_status fm_attn_fwd_varlen(const void* q, const void* k, const void* v,
  * Arguments as fm_attn_fwd_varlen (same meaning and rules).  The device
  * error word and timeout record of `workspace` are cleared.
  */
-FM_API fm_status fm_attn_fwd_plan(int64_t total_tokens, int n_heads_q, const int32_t* cu_seqlens,
-                                  int n_seqs, const int32_t* startend_row_indices,
-                                  int n_mask_heads, const int32_t* block_minmax, int causal,
-                                  int block_m, int block_n, void* workspace,
-                                  size_t workspace_bytes, void* stream);
+FM_API fm_status fm_attn_fwd_plan(int64_t total_tokens, int n_heads_q, int n_heads_kv,
+                                  const int32_t* cu_seqlens, int n_seqs,
+                                  const int32_t* startend_row_indices, int n_mask_heads,
+                                  const int32_t* block_minmax, int causal, int block_m,
+                                  int block_n, void* workspace, size_t workspace_bytes,
+                                  void* stream);
 
 /*
  * fm_attn_fwd_varlen_noalloc -- fm_attn_fwd_varlen for callers that cannot

@@ -76,8 +76,8 @@ _SIGNATURES = {
                                     _c_int, _c_vp, _c_int, _c_vp, _c_int, ctypes.c_float, _c_int,
                                     _c_int, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_u32,
                                     _c_vp]),
-    "fm_attn_fwd_plan": (_c_int, [_c_i64, _c_int, _c_vp, _c_int, _c_vp, _c_int, _c_vp, _c_int,
-                                  _c_int, _c_int, _c_vp, ctypes.c_size_t, _c_vp]),
+    "fm_attn_fwd_plan": (_c_int, [_c_i64, _c_int, _c_int, _c_vp, _c_int, _c_vp, _c_int, _c_vp,
+                                  _c_int, _c_int, _c_int, _c_vp, ctypes.c_size_t, _c_vp]),
     "fm_attn_fwd_varlen_noalloc": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_int, _c_int, _c_int,
                                             _c_vp, _c_int, _c_vp, _c_int, _c_vp, _c_int,
                                             ctypes.c_float, _c_int, _c_int, _c_vp, _c_vp, _c_vp,
@@ -274,7 +274,7 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
     return out, lse
 
 
-def attn_fwd_plan(cu_seqlens: torch.Tensor, total_tokens: int, n_heads_q: int,
+def attn_fwd_plan(cu_seqlens: torch.Tensor, total_tokens: int, n_heads_q: int, n_heads_kv: int,
                   startend_row_indices: Optional[torch.Tensor] = None,
                   block_minmax: Optional[torch.Tensor] = None, causal: bool = False,
                   block_m: int = 128, block_n: int = 128,
@@ -295,7 +295,8 @@ def attn_fwd_plan(cu_seqlens: torch.Tensor, total_tokens: int, n_heads_q: int,
         nbytes = attn_fwd_workspace_size(total_tokens, n_seqs, n_heads_q, block_m)
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=cu_seqlens.device)
     _check("fm_attn_fwd_plan", _lib().fm_attn_fwd_plan(
-        total_tokens, n_heads_q, _ptr(cu_seqlens), n_seqs, _ptr(startend_row_indices), hm,
+        total_tokens, n_heads_q, n_heads_kv, _ptr(cu_seqlens), n_seqs,
+        _ptr(startend_row_indices), hm,
         _ptr(block_minmax), int(bool(causal)), block_m, block_n, _ptr(workspace),
         workspace.numel(), _stream(stream)))
     return workspace

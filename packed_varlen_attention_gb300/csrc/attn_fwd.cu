@@ -10,21 +10,25 @@
 //
 // How it runs on GB300:
 //   * Planner (two tiny kernels, also callable alone so that the layers of
-//     one packed batch share one plan): one warp per sample-local pair of Q
-//     tiles counts the blocks that are not fully masked (its cost); one CTA
-//     orders the real pairs by cost, largest first (counting sort over cost
-//     bins), and writes the header (item count, the sizes planned for).
+//     one packed batch share one plan): one warp per planner slot (a Q tile,
+//     or a sample-local pair of Q tiles) counts the blocks that are not fully
+//     masked (its cost); one CTA orders the real slots by cost, largest first
+//     (counting sort over cost bins), and writes the header (item count, the
+//     sizes and item form planned for).
 //     Only real tiles become work -- not the fixed grid
 //     (seq_count, n_head, ceil(max_seq_len / Br)) of the Varlen-Packing
 //     technical document, section 2, whose CTAs past a short sample's end do
-//     nothing.  Pairs are formed from the sample's end, so a sample with an
-//     odd number of Q tiles leaves its first (under a causal mask cheapest)
-//     tile unpaired.
-//   * Persistent main kernel, one CTA per SM, pulling items (a pair of Q
-//     tiles of one sample x one q head) from an atomic counter; the last CTA
-//     to finish claiming resets the counter, so a plan can be used again.
-//     The two Q tiles share every K/V tile the CTA loads.  Warp roles (384
-//     threads; warps 0..3 at 96 registers, the softmax warpgroups at 200):
+//     nothing.
+//   * Persistent main kernel, one CTA per SM, pulling items from an atomic
+//     counter; the last CTA to finish claiming resets the counter, so a plan
+//     can be used again.  An item is two Q tiles that share every K/V tile
+//     the CTA loads: one Q tile for two q heads of one key/value head when
+//     the group size is even and every head has the same mask (both tiles
+//     then see the same blocks), else two consecutive Q tiles of one q head,
+//     paired from the sample's end so that a sample with an odd number of Q
+//     tiles leaves its first (under a causal mask cheapest) tile unpaired.
+//     Warp roles (384 threads; warps 0..3 at 96 registers, the softmax
+//     warpgroups at 200):
 //       warp 0      K producer: checks the plan's sizes, classifies the
 //                   item's KV tiles for both Q tiles (warp-parallel, 32 tiles
 //                   per step), loads Q tile 0 into the Q ring right after,
@@ -228,7 +232,8 @@ __device__ __forceinline__ int kv_tiles_to_scan(const AttnParams& p, int a, int 
 }
 
 // ---------------------------------------------------------------------------
-// planner: work unit = (sample, pair of consecutive Q tiles)
+// planner: work unit = (sample, Q tile) for head pairs, else (sample, pair
+// of consecutive Q tiles)
 // ---------------------------------------------------------------------------
 
 // Rows of item `pair` of the sample [a, b): Q tile 0 [r0, r1), Q tile 1
@@ -253,6 +258,20 @@ __device__ __forceinline__ void item_rows(int a, int b, int64_t pair, int bm, in
   r2 = single ? r1 : min(r0 + 2 * bm, b);
 }
 
+// Tile sizes and item form of a plan, as stored in the workspace header.
+__device__ __forceinline__ int plan_tiles_word(const AttnParams& p) {
+  return p.block_m | (p.block_n << 12) | (p.head_pairs << 24);
+}
+
+// Rows of the item of slot `tile` in head-pair form: one Q tile [r0, r1) for
+// two q heads (r2 = r1: no second row range).
+__device__ __forceinline__ void tile_rows(int a, int b, int64_t tile, int bm, int& r0, int& r1,
+                                          int& r2) {
+  r0 = static_cast<int>(min(static_cast<int64_t>(a) + tile * bm, static_cast<int64_t>(b)));
+  r1 = min(r0 + bm, b);
+  r2 = r1;
+}
+
 // The planner is two programmatic dependent launches (see launch_pdl): each
 // waits for the kernel before it, then lets the next one start launching,
 // so the attention kernel's set-up overlaps the planner.  Neither needs the
@@ -270,7 +289,8 @@ __global__ void __launch_bounds__(256) plan_cost_kernel(const AttnParams p) {
   const int lane = threadIdx.x & 31;
   if (u >= p.n_qslots) return;
   const int T = static_cast<int>(p.T);
-  const int BM2 = QT * p.block_m;  // rows of one item
+  const bool hpair = p.head_pairs != 0;
+  const int BM2 = (hpair ? 1 : QT) * p.block_m;  // rows of one slot
   int lo = 0, hi = p.n_seqs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -286,7 +306,10 @@ __global__ void __launch_bounds__(256) plan_cost_kernel(const AttnParams p) {
     return;
   }
   int r0, r1, r2;
-  item_rows<QT>(a, b, pair, p.block_m, r0, r1, r2);
+  if (hpair)
+    tile_rows(a, b, pair, p.block_m, r0, r1, r2);
+  else
+    item_rows<QT>(a, b, pair, p.block_m, r0, r1, r2);
   const int kt_end = kv_tiles_to_scan<BN>(p, a, b, r2);
   // With one mask per q head the pair's items differ in cost; the order
   // uses the costliest head's count (all heads of a pair run side by side).
@@ -376,7 +399,7 @@ __global__ void __launch_bounds__(kCostBins) plan_order_kernel(const AttnParams 
     AttnWorkspaceHeader* hd = p.ws;
     hd->work_counter = 0u;
     hd->n_qtiles = n_tiles;
-    hd->n_items = incl * p.hq;
+    hd->n_items = incl * (p.head_pairs ? p.hq / 2 : p.hq);
     hd->n_tile_items = n_tiles * p.hq;
     hd->error_word = bad ? static_cast<int>(FM_DEVERR_DATA) : 0;
 #pragma unroll
@@ -385,7 +408,7 @@ __global__ void __launch_bounds__(kCostBins) plan_order_kernel(const AttnParams 
     hd->plan_T = static_cast<int32_t>(p.T);
     hd->plan_n_seqs = p.n_seqs;
     hd->plan_hq = p.hq;
-    hd->plan_tiles = p.block_m | (p.block_n << 16);
+    hd->plan_tiles = plan_tiles_word(p);
   }
 }
 
@@ -445,7 +468,7 @@ __device__ __forceinline__ void attn_teardown(uint32_t* tmem_slot, int warp) {
 
 // Warps 0..3 (reduced register budget): K producer, MMA issuer, V producer
 // and one idle warp; warp 0 initialises the barriers, warp 1 owns TMEM.
-template <int D, int BN, int QT, typename IdxT, bool ROPE>
+template <int D, int BN, int QT, typename IdxT, bool ROPE, bool HP>
 __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const CUtensorMap& tq,
                                                     const CUtensorMap& tk,
                                                     const CUtensorMap& tv, const RopeArgs& ra) {
@@ -521,7 +544,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       const int4 h0 = *reinterpret_cast<const int4*>(p.ws);
       const int4 hp = *reinterpret_cast<const int4*>(&p.ws->plan_T);
       const bool fits = (hp.x == static_cast<int32_t>(p.T)) & (hp.y == p.n_seqs) &
-                        (hp.z == p.hq) & (hp.w == (p.block_m | (p.block_n << 16)));
+                        (hp.z == p.hq) & (hp.w == plan_tiles_word(p));
       if (!fits) {
         if (lane == 0) atomicOr(&p.ws->error_word, static_cast<int>(FM_DEVERR_DATA));
       } else if (!(p.reuse_plan && h0.w != 0)) {
@@ -531,6 +554,10 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       }
     }
     const int group = p.hq / p.hkv;
+    // head-pair items: one Q tile for q heads 2k and 2k + 1 (one key/value
+    // head, one mask); otherwise two Q tiles of one q head
+    constexpr bool hpair = HP;
+    const int per_slot = hpair ? p.hq / 2 : p.hq;  // items per planner slot
     constexpr uint32_t NKV = kKVSlots<BN>, NQ = kQSlots<BN>;
     uint32_t kv_t = 0;               // KV tiles loaded (K(t) is ring load 2t)
     uint32_t mslot = 0, mround = 0;  // metadata ring
@@ -651,8 +678,8 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
         ok = push_meta(kStop, kClsF, kClsF, 0, 0, 0, 0, 0, 0, false, 0, 0, 0u);
         break;
       }
-      const int2 pi = p.order[item / p.hq];
-      const int h = item % p.hq;
+      const int2 pi = p.order[item / per_slot];
+      const int h = hpair ? 2 * (item % per_slot) : item % per_slot;
       // an entry the planner never writes becomes an empty item (no rows)
       const bool bad_entry = pi.x < 0 || pi.x >= p.n_seqs || pi.y < 0;
       if (bad_entry && lane == 0) atomicOr(&p.ws->error_word, static_cast<int>(FM_DEVERR_DATA));
@@ -662,8 +689,13 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       const int a = clamp_tok(__ldg(p.cu + s), T);
       const int b = max(a, clamp_tok(__ldg(p.cu + s + 1), T));
       int r0, r1, r2;
-      item_rows<QT>(a, b, bad_entry ? (1 << 30) : pi.y, BM, r0, r1, r2);
-      const bool has_q1 = r2 > r1;  // (never with one Q tile per item)
+      if (hpair)
+        tile_rows(a, b, bad_entry ? (1 << 30) : pi.y, BM, r0, r1, r2);
+      else
+        item_rows<QT>(a, b, bad_entry ? (1 << 30) : pi.y, BM, r0, r1, r2);
+      // the item's second Q tile: the next q head's (head pairs) or the next
+      // rows' (never with one Q tile per item)
+      const bool has_q1 = hpair ? r1 > r0 : r2 > r1;
       const int n_kv = (b - a + BN - 1) / BN;
       const int kt_end = (r2 > r0) ? kv_tiles_to_scan<BN>(p, a, b, r2) : 0;
 
@@ -672,6 +704,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       for (int base = 0; base < kt_end; base += 32) {
         int c0, c1;
         tile_classes<BN>(p, mh, s, a, b, r0, r1, r2, base + lane, kt_end, c0, c1);
+        if (hpair) c1 = has_q1 ? c0 : kClsF;  // the same rows and mask
         n_live += __popc(__ballot_sync(0xffffffffu, c0 != kClsF || c1 != kClsF));
         const int p0 = __popc(__ballot_sync(0xffffffffu, c0 == kClsP || c0 == kClsPC));
         const int u0 = __popc(__ballot_sync(0xffffffffu, c0 == kClsU));
@@ -684,37 +717,41 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       if (r2 > r0) cnt_f += static_cast<long long>(n_kv) * (has_q1 ? 2 : 1);
 
       if (n_live == 0) {
-        // every key of these rows is masked: o = 0, lse = -inf
-        for (int r = r0 + lane; r < r2; r += 32) {
-          uint4* dst = reinterpret_cast<uint4*>(
-              static_cast<__nv_bfloat16*>(p.out) +
-              (static_cast<IdxT>(r) * p.hq + h) * static_cast<IdxT>(D));
+        // every key of these rows is masked: o = 0, lse = -inf (for both q
+        // heads of a head-pair item)
+        const int h_end = h + ((hpair && has_q1) ? 2 : 1);
+        for (int hh = h; hh < h_end; ++hh) {
+          for (int r = r0 + lane; r < r2; r += 32) {
+            uint4* dst = reinterpret_cast<uint4*>(
+                static_cast<__nv_bfloat16*>(p.out) +
+                (static_cast<IdxT>(r) * p.hq + hh) * static_cast<IdxT>(D));
 #pragma unroll
-          for (int u = 0; u < D / 8; ++u) dst[u] = make_uint4(0u, 0u, 0u, 0u);
-          p.lse[static_cast<IdxT>(h) * static_cast<IdxT>(p.T) + r] = -CUDART_INF_F;
-        }
-        if constexpr (ROPE) {
-          // no Q tile of these rows is loaded: rotate them from q directly
-          if (ra.q_rot != nullptr) {
-            constexpr int kG = D / 16;  // chunk pairs per row
-            for (int idx = lane; idx < (r2 - r0) * kG; idx += 32) {
-              const int r = r0 + idx / kG;
-              const int g = idx % kG;
-              const IdxT off = (static_cast<IdxT>(r) * p.hq + h) * static_cast<IdxT>(D) + g * 8;
-              const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(p.q) + off;
-              __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(ra.q_rot) + off;
-              const uint4 x1 = *reinterpret_cast<const uint4*>(src);
-              const uint4 x2 = *reinterpret_cast<const uint4*>(src + D / 2);
-              const float pos = static_cast<float>(r - a);
-              float cs[8], sn[8];
+            for (int u = 0; u < D / 8; ++u) dst[u] = make_uint4(0u, 0u, 0u, 0u);
+            p.lse[static_cast<IdxT>(hh) * static_cast<IdxT>(p.T) + r] = -CUDART_INF_F;
+          }
+          if constexpr (ROPE) {
+            // no Q tile of these rows is loaded: rotate them from q directly
+            if (ra.q_rot != nullptr) {
+              constexpr int kG = D / 16;  // chunk pairs per row
+              for (int idx = lane; idx < (r2 - r0) * kG; idx += 32) {
+                const int r = r0 + idx / kG;
+                const int g = idx % kG;
+                const IdxT off = (static_cast<IdxT>(r) * p.hq + hh) * static_cast<IdxT>(D) + g * 8;
+                const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(p.q) + off;
+                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(ra.q_rot) + off;
+                const uint4 x1 = *reinterpret_cast<const uint4*>(src);
+                const uint4 x2 = *reinterpret_cast<const uint4*>(src + D / 2);
+                const float pos = static_cast<float>(r - a);
+                float cs[8], sn[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                rope_cos_sin(pos, ra.freqs.hi[g * 8 + i], ra.freqs.lo[g * 8 + i], 1.0f, cs[i],
-                             sn[i]);
-              uint4 y1, y2;
-              rope_rotate8(x1, x2, cs, sn, y1, y2);
-              *reinterpret_cast<uint4*>(dst) = y1;
-              *reinterpret_cast<uint4*>(dst + D / 2) = y2;
+                for (int i = 0; i < 8; ++i)
+                  rope_cos_sin(pos, ra.freqs.hi[g * 8 + i], ra.freqs.lo[g * 8 + i], 1.0f, cs[i],
+                               sn[i]);
+                uint4 y1, y2;
+                rope_rotate8(x1, x2, cs, sn, y1, y2);
+                *reinterpret_cast<uint4*>(dst) = y1;
+                *reinterpret_cast<uint4*>(dst + D / 2) = y2;
+              }
             }
           }
         }
@@ -737,6 +774,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
       for (int base = 0; base < kt_end && ok; base += 32) {
         int my0, my1;
         tile_classes<BN>(p, mh, s, a, b, r0, r1, r2, base + lane, kt_end, my0, my1);
+        if (hpair) my1 = has_q1 ? my0 : kClsF;
         uint32_t live = __ballot_sync(0xffffffffu, my0 != kClsF || my1 != kClsF);
         while (live != 0u) {
           const int l = __ffs(live) - 1;
@@ -771,7 +809,7 @@ __device__ __forceinline__ void attn_producer_roles(const AttnParams& p, const C
             ++kv_t;
           }
           if (pushed == 0) {
-            if (has_q1 && !load_q(q_seq + 1u, h, r0 + BM)) {
+            if (has_q1 && !load_q(q_seq + 1u, hpair ? h + 1 : h, hpair ? r0 : r0 + BM)) {
               ok = false;
               break;
             }
@@ -1202,7 +1240,7 @@ __device__ __forceinline__ void store_q_tile(const AttnParams& p, const RopeArgs
   }
 }
 
-template <int D, int BN, int QT, typename IdxT, bool ROPE>
+template <int D, int BN, int QT, typename IdxT, bool ROPE, bool HP>
 __device__ __forceinline__ void attn_softmax_role(const AttnParams& p, const RopeArgs& ra) {
   using L = Layout<D, BN, QT>;
   extern __shared__ uint8_t smem_raw[];
@@ -1337,8 +1375,9 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p, const Rop
       // the previous item is done)
       int n_h = h, n_rt0 = rt0, n_rt1 = rt1;
       if (first) {
-        n_h = mb.w;
-        n_rt0 = mb.y + wg * BM;
+        // head pairs: the same rows, head h + wg; otherwise rows r0 + wg * BM
+        n_h = mb.w + (HP ? wg : 0);
+        n_rt0 = mb.y + (HP ? 0 : wg * BM);
         n_rt1 = min(n_rt0 + BM, mb.z);
         if constexpr (ROPE) {
           // the Q ring position of this warpgroup's tile (read before the
@@ -1585,7 +1624,7 @@ __device__ __forceinline__ void attn_softmax_role(const AttnParams& p, const Rop
   }
 }
 
-template <int D, int BN, int QT, typename IdxT, bool ROPE>
+template <int D, int BN, int QT, typename IdxT, bool ROPE, bool HP>
 __global__ void __launch_bounds__(kThreads<QT>, 1)
     attn_fwd_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tq,
                     const __grid_constant__ CUtensorMap tk,
@@ -1595,10 +1634,10 @@ __global__ void __launch_bounds__(kThreads<QT>, 1)
   // into the other.
   if ((threadIdx.x >> 5) < 4) {
     if constexpr (QT == 2) regs_release();
-    attn_producer_roles<D, BN, QT, IdxT, ROPE>(p, tq, tk, tv, ra);
+    attn_producer_roles<D, BN, QT, IdxT, ROPE, HP>(p, tq, tk, tv, ra);
   } else {
     if constexpr (QT == 2) regs_acquire();
-    attn_softmax_role<D, BN, QT, IdxT, ROPE>(p, ra);
+    attn_softmax_role<D, BN, QT, IdxT, ROPE, HP>(p, ra);
   }
 }
 
@@ -1624,7 +1663,7 @@ cudaError_t launch_plan(const AttnParams& p, cudaStream_t stream) {
   return launch_pdl(plan_order_kernel, dim3(1), dim3(kCostBins), 0, stream, p);
 }
 
-template <int D, int BN, int QT, typename IdxT, bool ROPE>
+template <int D, int BN, int QT, typename IdxT, bool ROPE, bool HP>
 cudaError_t launch_typed(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const RopeArgs& ra, int num_sms,
                          cudaStream_t stream) {
@@ -1637,11 +1676,11 @@ cudaError_t launch_typed(const AttnParams& p, const CUtensorMap& tq, const CUten
     // The warpgroups' register split must fit in what the launch allocates,
     // or setmaxnreg.inc would wait forever: refuse to launch otherwise.
     cudaFuncAttributes attr;
-    e = cudaFuncGetAttributes(&attr, attn_fwd_kernel<D, BN, QT, IdxT, ROPE>);
+    e = cudaFuncGetAttributes(&attr, attn_fwd_kernel<D, BN, QT, IdxT, ROPE, HP>);
     if (e != cudaSuccess) return e;
     if (QT == 2 && attr.numRegs * kThreads<QT> < kProducerRegs * 128 + kSoftmaxRegs * 256)
       return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(attn_fwd_kernel<D, BN, QT, IdxT, ROPE>,
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D, BN, QT, IdxT, ROPE, HP>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
     if (dev < 64) configured |= 1ull << dev;
@@ -1653,7 +1692,7 @@ cudaError_t launch_typed(const AttnParams& p, const CUtensorMap& tq, const CUten
   }
   const int64_t max_items = n_slots * p.hq;
   const int grid = static_cast<int>(max_items < num_sms ? max_items : num_sms);
-  return launch_pdl(attn_fwd_kernel<D, BN, QT, IdxT, ROPE>, dim3(grid), dim3(kThreads<QT>),
+  return launch_pdl(attn_fwd_kernel<D, BN, QT, IdxT, ROPE, HP>, dim3(grid), dim3(kThreads<QT>),
                     L::kBytes, stream, p, tq, tk, tv, ra);
 }
 
@@ -1668,24 +1707,35 @@ size_t attn_workspace_bytes(int64_t T, int n_seqs, int block_m) {
 
 namespace {
 
+// HP: work items of one Q tile for two q heads (head pairs), else two Q
+// tiles of one q head.
+template <bool ROPE, bool HP>
+cudaError_t launch_attn_dispatch_hp(const AttnParams& p, const CUtensorMap& tq,
+                                    const CUtensorMap& tk, const CUtensorMap& tv,
+                                    const RopeArgs& ra, bool use_int64, int num_sms,
+                                    cudaStream_t stream) {
+  constexpr int Q2 = kQTilesBN128;
+  if (p.head_dim == 128) {
+    if (p.block_n == 128)
+      return use_int64 ? launch_typed<128, 128, Q2, int64_t, ROPE, HP>(p, tq, tk, tv, ra, num_sms, stream)
+                       : launch_typed<128, 128, Q2, int32_t, ROPE, HP>(p, tq, tk, tv, ra, num_sms, stream);
+    return use_int64 ? launch_typed<128, 64, 2, int64_t, ROPE, HP>(p, tq, tk, tv, ra, num_sms, stream)
+                     : launch_typed<128, 64, 2, int32_t, ROPE, HP>(p, tq, tk, tv, ra, num_sms, stream);
+  }
+  if (p.block_n == 128)
+    return use_int64 ? launch_typed<64, 128, Q2, int64_t, ROPE, HP>(p, tq, tk, tv, ra, num_sms, stream)
+                     : launch_typed<64, 128, Q2, int32_t, ROPE, HP>(p, tq, tk, tv, ra, num_sms, stream);
+  return use_int64 ? launch_typed<64, 64, 2, int64_t, ROPE, HP>(p, tq, tk, tv, ra, num_sms, stream)
+                   : launch_typed<64, 64, 2, int32_t, ROPE, HP>(p, tq, tk, tv, ra, num_sms, stream);
+}
+
 template <bool ROPE>
 cudaError_t launch_attn_dispatch(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                                  const CUtensorMap& tv, const RopeArgs& ra, bool use_int64,
                                  int num_sms, cudaStream_t stream) {
-  if (p.head_dim == 128) {
-    if (p.block_n == 128)
-      return use_int64
-                 ? launch_typed<128, 128, kQTilesBN128, int64_t, ROPE>(p, tq, tk, tv, ra, num_sms, stream)
-                 : launch_typed<128, 128, kQTilesBN128, int32_t, ROPE>(p, tq, tk, tv, ra, num_sms, stream);
-    return use_int64 ? launch_typed<128, 64, 2, int64_t, ROPE>(p, tq, tk, tv, ra, num_sms, stream)
-                     : launch_typed<128, 64, 2, int32_t, ROPE>(p, tq, tk, tv, ra, num_sms, stream);
-  }
-  if (p.block_n == 128)
-    return use_int64
-               ? launch_typed<64, 128, kQTilesBN128, int64_t, ROPE>(p, tq, tk, tv, ra, num_sms, stream)
-               : launch_typed<64, 128, kQTilesBN128, int32_t, ROPE>(p, tq, tk, tv, ra, num_sms, stream);
-  return use_int64 ? launch_typed<64, 64, 2, int64_t, ROPE>(p, tq, tk, tv, ra, num_sms, stream)
-                   : launch_typed<64, 64, 2, int32_t, ROPE>(p, tq, tk, tv, ra, num_sms, stream);
+  return p.head_pairs
+             ? launch_attn_dispatch_hp<ROPE, true>(p, tq, tk, tv, ra, use_int64, num_sms, stream)
+             : launch_attn_dispatch_hp<ROPE, false>(p, tq, tk, tv, ra, use_int64, num_sms, stream);
 }
 
 }  // namespace

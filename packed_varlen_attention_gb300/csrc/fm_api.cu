@@ -207,7 +207,7 @@ void rope_freqs(double theta, int head_dim, fm::RopeFreqs* fr) {
 // The scheduler's part of the forward parameters: samples, mask statistics,
 // tile sizes and the workspace tables (shared by the attention calls and
 // fm_attn_fwd_plan, so that a plan and the calls that reuse it agree).
-void set_schedule_params(AttnParams& p, int64_t total_tokens, int n_heads_q,
+void set_schedule_params(AttnParams& p, int64_t total_tokens, int n_heads_q, int n_heads_kv,
                          const int32_t* cu_seqlens, int n_seqs,
                          const int32_t* startend_row_indices, int n_mask_heads,
                          const int32_t* block_minmax, int causal, int block_m, int block_n,
@@ -227,22 +227,28 @@ void set_schedule_params(AttnParams& p, int64_t total_tokens, int n_heads_q,
   p.n_kv_slots = fm_num_kv_tiles_bound(total_tokens, n_seqs, block_n);
   p.n_seqs = n_seqs;
   p.hq = n_heads_q;
+  p.hkv = n_heads_kv;
   p.hm = n_mask_heads;
   p.block_m = block_m;
   p.block_n = block_n;
   p.causal = causal != 0;
+  // Work items of two q heads that share a key/value head and the mask (one
+  // Q tile each): both softmax warpgroups then see the same blocks, where two
+  // consecutive Q tiles of one head differ in their last key tiles.
+  p.head_pairs = n_mask_heads <= 1 && (n_heads_q / n_heads_kv) % 2 == 0;
 }
 
 // Validation shared by the attention forward calls and fm_attn_fwd_plan:
 // samples, mask arguments (n_mask_heads is set to 0 without a mask), tile
 // sizes and workspace.
-fm_status check_schedule_args(int64_t total_tokens, int n_heads_q, const int32_t* cu_seqlens,
-                              int n_seqs, const int32_t* startend_row_indices,
+fm_status check_schedule_args(int64_t total_tokens, int n_heads_q, int n_heads_kv,
+                              const int32_t* cu_seqlens, int n_seqs,
+                              const int32_t* startend_row_indices,
                               int& n_mask_heads, const int32_t* block_minmax, int block_m,
                               int block_n, const void* workspace, size_t workspace_bytes) {
   if (cu_seqlens == nullptr || workspace == nullptr) return FM_ERR_INVALID_ARG;
   if (total_tokens < 0 || total_tokens > INT32_MAX - 256 || n_seqs < 1) return FM_ERR_INVALID_ARG;
-  if (n_heads_q < 1) return FM_ERR_INVALID_ARG;
+  if (n_heads_q < 1 || n_heads_kv < 1 || n_heads_q % n_heads_kv != 0) return FM_ERR_INVALID_ARG;
   if (startend_row_indices != nullptr) {
     if (n_mask_heads != 1 && n_mask_heads != n_heads_q) return FM_ERR_INVALID_ARG;
     if (block_minmax == nullptr) return FM_ERR_INVALID_ARG;
@@ -278,9 +284,8 @@ fm_status attn_fwd_impl(const void* q, void* k_rot_in_place, const void* k, cons
   if (q_rot != nullptr && !aligned(q_rot, 16)) return FM_ERR_ALIGNMENT;
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || lse == nullptr)
     return FM_ERR_INVALID_ARG;
-  if (n_heads_kv < 1 || n_heads_q < 1 || n_heads_q % n_heads_kv != 0) return FM_ERR_INVALID_ARG;
   if (flags & ~(FM_FLAG_FORCE_INT64 | FM_FLAG_REUSE_PLAN)) return FM_ERR_INVALID_ARG;
-  fm_status st = check_schedule_args(total_tokens, n_heads_q, cu_seqlens, n_seqs,
+  fm_status st = check_schedule_args(total_tokens, n_heads_q, n_heads_kv, cu_seqlens, n_seqs,
                                      startend_row_indices, n_mask_heads, block_minmax, block_m,
                                      block_n, workspace, workspace_bytes);
   if (st != FM_OK) return st;
@@ -304,15 +309,15 @@ fm_status attn_fwd_impl(const void* q, void* k_rot_in_place, const void* k, cons
 
   AttnParams p;
   std::memset(&p, 0, sizeof(p));
-  set_schedule_params(p, total_tokens, n_heads_q, cu_seqlens, n_seqs, startend_row_indices,
-                      n_mask_heads, block_minmax, causal, block_m, block_n, workspace);
+  set_schedule_params(p, total_tokens, n_heads_q, n_heads_kv, cu_seqlens, n_seqs,
+                      startend_row_indices, n_mask_heads, block_minmax, causal, block_m, block_n,
+                      workspace);
   p.q = q;
   p.k = k;
   p.v = v;
   p.out = out;
   p.lse = lse;
   p.class_counts = block_class_counts;
-  p.hkv = n_heads_kv;
   p.head_dim = head_dim;
   p.reuse_plan = (flags & FM_FLAG_REUSE_PLAN) != 0;
   const double scale = softmax_scale > 0.0f ? softmax_scale : 1.0 / std::sqrt(double(head_dim));
@@ -374,11 +379,12 @@ fm_status fm_attn_fwd_varlen_rope(const void* q, void* k, const void* v, int64_t
                        block_class_counts, workspace, workspace_bytes, flags, stream);
 }
 
-fm_status fm_attn_fwd_plan(int64_t total_tokens, int n_heads_q, const int32_t* cu_seqlens,
-                           int n_seqs, const int32_t* startend_row_indices, int n_mask_heads,
+fm_status fm_attn_fwd_plan(int64_t total_tokens, int n_heads_q, int n_heads_kv,
+                           const int32_t* cu_seqlens, int n_seqs,
+                           const int32_t* startend_row_indices, int n_mask_heads,
                            const int32_t* block_minmax, int causal, int block_m, int block_n,
                            void* workspace, size_t workspace_bytes, void* stream) {
-  fm_status st = check_schedule_args(total_tokens, n_heads_q, cu_seqlens, n_seqs,
+  fm_status st = check_schedule_args(total_tokens, n_heads_q, n_heads_kv, cu_seqlens, n_seqs,
                                      startend_row_indices, n_mask_heads, block_minmax, block_m,
                                      block_n, workspace, workspace_bytes);
   if (st != FM_OK) return st;
@@ -388,8 +394,9 @@ fm_status fm_attn_fwd_plan(int64_t total_tokens, int n_heads_q, const int32_t* c
   if (st != FM_OK) return st;
   AttnParams p;
   std::memset(&p, 0, sizeof(p));
-  set_schedule_params(p, total_tokens, n_heads_q, cu_seqlens, n_seqs, startend_row_indices,
-                      n_mask_heads, block_minmax, causal, block_m, block_n, workspace);
+  set_schedule_params(p, total_tokens, n_heads_q, n_heads_kv, cu_seqlens, n_seqs,
+                      startend_row_indices, n_mask_heads, block_minmax, causal, block_m, block_n,
+                      workspace);
   return from_cuda(fm::launch_attn_plan(p, static_cast<cudaStream_t>(stream)));
 }
 

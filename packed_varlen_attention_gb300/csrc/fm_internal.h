@@ -71,7 +71,8 @@ struct AttnWorkspaceHeader {
   int32_t bwd_q_tiles;       // backward: real 128-row tiles (planner)
   int32_t bwd_kv_tiles;      // backward: the same count for the key/value pass
   // forward plan: the sizes it was made for (plan_n_seqs = 0: no valid plan),
-  // one 16-byte group read with one load; plan_tiles = block_m | block_n << 16
+  // one 16-byte group read with one load; plan_tiles = block_m | block_n << 12
+  // | head_pairs << 24
   int32_t plan_T, plan_n_seqs, plan_hq, plan_tiles;
   uint32_t exit_counter;  // forward: CTAs done claiming (the last one resets the counters)
   int32_t pad[47];
@@ -107,6 +108,7 @@ struct AttnParams {
   int block_m, block_n;
   int causal;
   int reuse_plan;  // skip the planner: the workspace holds the work order already
+  int head_pairs;  // a work item is one Q tile for two q heads of one key/value head
   float scale_log2;
   uint64_t timeout_ns;
 };

@@ -30,8 +30,8 @@ int main(void) {
                                 NULL, 0, NULL, 1, 0.0f, 128, 128, fake, (float*)fake, NULL, NULL,
                                 fake, 1 << 20, 0, NULL) == FM_ERR_INVALID_ARG);
   /* a plan needs a workspace of fm_attn_fwd_workspace_size bytes */
-  CHECK(fm_attn_fwd_plan(8192, 32, (const int32_t*)fake, 8, NULL, 0, NULL, 1, 128, 128, fake, 64,
-                         NULL) == FM_ERR_WORKSPACE);
+  CHECK(fm_attn_fwd_plan(8192, 32, 8, (const int32_t*)fake, 8, NULL, 0, NULL, 1, 128, 128, fake,
+                         64, NULL) == FM_ERR_WORKSPACE);
   printf("ok %s\n", fm_status_string(FM_ERR_WORKSPACE));
   return 0;
 }

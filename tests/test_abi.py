@@ -112,13 +112,15 @@ def test_validation_rejects_before_any_launch(fm):
     assert attn_rope(q_rot=ctypes.c_void_p(0x10008)) == 3
     assert attn_rope(hq=3) == 1
     # the scheduler alone: the same sample, mask, tile and workspace rules
-    def plan(cu=fake, hq=4, sri=None, hm=0, mm=None, bm=128, bn=128, ws=fake, ws_bytes=1 << 20,
-             T=256):
-        return lib.fm_attn_fwd_plan(T, hq, cu, 2, sri, hm, mm, 1, bm, bn, ws, ws_bytes, None)
+    def plan(cu=fake, hq=4, hkv=2, sri=None, hm=0, mm=None, bm=128, bn=128, ws=fake,
+             ws_bytes=1 << 20, T=256):
+        return lib.fm_attn_fwd_plan(T, hq, hkv, cu, 2, sri, hm, mm, 1, bm, bn, ws, ws_bytes, None)
     assert plan(cu=None) == 1
     assert plan(ws=None) == 1
     assert plan(T=-1) == 1
     assert plan(hq=0) == 1
+    assert plan(hq=4, hkv=3) == 1
+    assert plan(hkv=0) == 1
     assert plan(sri=fake, hm=3, mm=fake) == 1
     assert plan(sri=fake, hm=1, mm=None) == 1
     assert plan(bm=96) == 2

@@ -51,7 +51,8 @@ class Batch:
 
     def plan(self, fm, workspace=None):
         wl = self.wl
-        return fm.attn_fwd_plan(self.cu, wl.total_tokens, wl.n_heads_q, self.sri, self.mm,
+        return fm.attn_fwd_plan(self.cu, wl.total_tokens, wl.n_heads_q, wl.n_heads_kv,
+                                self.sri, self.mm,
                                 causal=wl.causal, block_m=wl.block_m, block_n=wl.block_n,
                                 workspace=workspace)
 
@@ -193,7 +194,7 @@ def test_plan_from_malformed_cu_seqlens_is_not_reused(fm):
                          mask="none", causal=True, seed=13)
     b = Batch(fm, wl, n_layers=1)
     bad = torch.tensor([0, 600, 300, 1000], dtype=torch.int32, device="cuda")
-    ws = fm.attn_fwd_plan(bad, wl.total_tokens, 4, causal=True)
+    ws = fm.attn_fwd_plan(bad, wl.total_tokens, 4, 2, causal=True)
     q, k, v = b.layers[0]
     out = torch.full_like(q, 7.0)
     fm.attn_fwd_varlen(q, k, v, bad, causal=True, out=out, workspace=ws, reuse_plan=True)
